@@ -1,0 +1,84 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins catch each one.
+
+Every mutant is a one-expression change to oracle/moe_oracle.c (a wrong index,
+an off-by-one, a dropped term, a wrong constant, truncation instead of
+rounding). It is compiled on the CPU, swapped in for the real oracle, and the
+pin tests of test_oracle_pins.py are run against it until one fails.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+# (name, original text, planted mistake); each original must occur exactly once
+MUTANTS = [
+    ("region transposed", "int64_t region = (int64_t)e * R + src;", "int64_t region = (int64_t)src * E + e;"),
+    ("slot position off by one", "int pos = counts[region]++;", "int pos = ++counts[region];"),
+    ("flag without the +1", "flags[r] = (uint64_t)counts[r] + 1;", "flags[r] = (uint64_t)counts[r];"),
+    ("duplicate check skipped", "if (row[jj] == e) return ORC_EINVAL;", "if (row[jj] == e + E) return ORC_EINVAL;"),
+    ("header token and choice swapped", "meta[out * 4 + 3] = j;", "meta[out * 4 + 3] = t;"),
+    ("scale block index wrong", "scales[i * nsc + h / 128]", "scales[i * nsc + h % nsc]"),
+    ("expert factor wrong", "double c = 1.0 + (double)e / 256.0;", "double c = 1.0 + (double)e / 128.0;"),
+    ("weight of the wrong choice", "double w = (double)weights[tok * k + j];",
+     "double w = (double)weights[tok * k + (k - 1 - j)];"),
+    ("one expert dropped", "acc[h] += w * orc_bf16_value(yr[h]);", "acc[h] += (j ? w : 0.0) * orc_bf16_value(yr[h]);"),
+    ("truncation instead of rounding", "double r = rint(a / quantum) * quantum;",
+     "double r = floor(a / quantum) * quantum;"),
+    ("bf16 subnormal spacing", "if (e < -126) e = -126;", "if (e < -140) e = -140;"),
+    ("e4m3 exponent bias", "v = ldexp((double)(8 + m), ex - 10);", "v = ldexp((double)(8 + m), ex - 9);"),
+    ("e4m3 subnormal scale", "v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
+    ("header bytes dropped", "out[2] = slots * 16;", "out[2] = slots * 4;"),
+    ("T > max_m accepted", "if (T > max_m) return ORC_EINVAL;", "if (T > 2 * max_m) return ORC_EINVAL;"),
+]
+
+# the pins, cheapest first; each takes the (unused) oracle_lib fixture value
+PINS = [
+    lambda: pins.test_validate(None),
+    lambda: pins.test_bf16_ties_go_to_even(None),
+    lambda: pins.test_e4m3_decode_matches_torch(None),
+    lambda: pins.test_bf16_rounding_matches_torch_on_float32_inputs(None),
+    lambda: pins.test_buffer_sizes_reproduce_the_printed_estimates(None),
+    lambda: pins.test_layout_rejects_bad_routing(None),
+    lambda: pins.test_layout_overflow_errors_out(None),
+    lambda: pins.test_layout_matches_brute_force(None, 3, 7, 6, 3, 9, 1),
+    lambda: pins.test_dispatch_slots_hold_source_rows(None, "tiny"),
+    lambda: pins.test_dispatch_fp8_carries_scales(None),
+    lambda: pins.test_expert_stub_is_the_nearest_bf16(None),
+    lambda: pins.test_combine_identity_experts_return_the_input(None),
+    lambda: pins.test_combine_scaling_experts_closed_form(None),
+    lambda: pins.test_combine_is_linear_in_the_weights(None),
+]
+
+
+def test_every_mutant_site_exists_once():
+    src = oracle.source()
+    for name, old, _ in MUTANTS:
+        assert src.count(old) == 1, name
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    oracle._load()
+    real = oracle._lib
+    lib_path = str(tmp_path / "liboracle_mutant.so")
+    oracle.compile_variant(oracle.source().replace(old, new), lib_path)
+    oracle._lib = oracle._bind(lib_path)
+    caught = None
+    try:
+        for i, pin in enumerate(PINS):
+            try:
+                with np.errstate(all="ignore"):
+                    pin()
+            except (AssertionError, oracle.OracleError, pytest.fail.Exception, ValueError, IndexError, KeyError) as e:
+                caught = (i, type(e).__name__)
+                break
+    finally:
+        oracle._lib = real
+    assert caught is not None, f"no pin caught the mutant '{name}'"
+
+
+def test_real_oracle_passes_the_same_pins():
+    oracle._load()
+    for pin in PINS:
+        pin()
