@@ -1,0 +1,460 @@
+#!/usr/bin/env python
+"""Benchmark of MoE expert-parallel dispatch + combine on GB300.
+
+One step = layout -> dispatch -> combine over one batch of the DeepSeek-shape
+decode workload (8 logical EP ranks x 128 tokens, hidden 7168 fp8 e4m3 with
+128-element fp32 scales, 256 experts, top-8, max_m 128), inputs resident in
+HBM. The synthetic experts run once before timing (their outputs stay
+resident; layout is deterministic, so every step gathers valid rows). L2 is
+flushed (a memset of twice its size) before every timed step, outside the
+timed events.
+
+Arms:
+  --impl native (default): the CUDA library through its C ABI; prints one JSON
+    line with the device-timed value, the end-to-end value (host buffers,
+    copies inside the timed region), the roofline of the dominant kernel
+    (combine), the CPU oracle baseline, clocks and launch counts.
+  --impl reference: the CPU oracle on the host cores, each step a bounded
+    sample of the same workload.
+
+Multi-GPU (torchrun): every rank runs an independent replica (no collective
+on the data path); rank 0 prints the whole-job value = all ranks' tokens /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine tokens/s and achieved HBM GB/s vs 8 TB/s, H=7168 top-8/256"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_WORKLOAD = "ds_decode"
+
+
+# --- process group ------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_over_ranks(value: float, world: int, op: str, device=None) -> float:
+    """max or sum of a per-rank float over all ranks (identity on one rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def whole_job(tokens_per_rank_step: int, local_ms_total: float, steps: int, world: int, device=None) -> dict:
+    """Whole-job throughput: tokens of all ranks over the slowest rank's time."""
+    slow_ms = reduce_over_ranks(local_ms_total, world, "max", device)
+    tokens = reduce_over_ranks(tokens_per_rank_step * steps, world, "sum", device)
+    return {"value": tokens / (slow_ms / 1e3), "ms_per_step": slow_ms / steps, "tokens": tokens}
+
+
+# --- clocks ------------------------------------------------------------------
+
+CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "utilization.gpu", "clocks_event_reasons.hw_slowdown",
+                "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+                "clocks_event_reasons.sw_power_cap"]
+REASON_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) while the GPU works."""
+
+    def __init__(self, local_rank: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        self.gpu = vis.split(",")[local_rank] if vis else str(local_rank)
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={','.join(CLOCK_FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(CLOCK_FIELDS):
+                self.samples.append(parts)
+
+    def stop(self) -> dict:
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        busy = [s for s in self.samples if (num(s[3]) or 0) > 0] or self.samples
+        sm = [num(s[0]) for s in busy if num(s[0]) is not None]
+        mx = [num(s[1]) for s in self.samples if num(s[1]) is not None]
+        reasons = sorted({REASON_NAMES[i] for s in busy for i in range(4) if s[4 + i].lower() == "active"})
+        power = [num(s[2]) for s in busy if num(s[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples), "busy_samples": len(busy) if sm else 0,
+                "power_w_max": max(power) if power else None}
+
+
+# --- roofline inputs ------------------------------------------------------------
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError, TypeError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash(name: str) -> str:
+    with open(os.path.join(ROOT, "combine_moe_layout_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_file.replace('.cu', '')}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(kernel_file):
+        return None
+    return float(m_bytes.group(1))
+
+
+# --- native arm -------------------------------------------------------------------
+
+def run_native(args, rank, local_rank, world):
+    import numpy as np
+    import torch
+
+    from combine_moe_layout_gb300 import _binding as B
+    from combine_moe_layout_gb300 import pipeline as P
+    from combine_moe_layout_gb300 import workloads as wl
+
+    assert torch.cuda.is_available(), "the native arm needs a CUDA device"
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    init_dist(world, "nccl")
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w)
+    step = P.MoeStep(w, dev, args.num_sms)
+    d = P.to_device(inp, dev)
+    stream = torch.cuda.current_stream()
+    step.reset()
+    step.run(d)  # also runs the synthetic experts once; their outputs stay resident
+    status = step.error()
+    if status != B.MOE_OK:
+        raise RuntimeError(f"first step failed: {B.moe_status_string(status)}")
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def path():
+        step.layout(d)
+        step.dispatch(d)
+        step.combine(d)
+
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        flush.zero_()
+        path()
+    torch.cuda.synchronize()
+    barrier(world)
+
+    sampler = ClockSampler(local_rank).start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize()
+    barrier(world)
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        path()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # per-kernel durations, CUDA events on the launching stream (a second pass of K steps)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        kev[i][0].record(stream)
+        step.layout(d)
+        kev[i][1].record(stream)
+        step.dispatch(d)
+        kev[i][2].record(stream)
+        step.combine(d)
+        kev[i][3].record(stream)
+    torch.cuda.synchronize()
+    kern_ms = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in kev)
+               for j, name in enumerate(("layout", "dispatch", "combine"))}
+
+    # end to end: host inputs in pinned memory, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.from_numpy(np.ascontiguousarray(inp.x)).pin_memory()
+        hidx = torch.from_numpy(inp.topk_idx).pin_memory()
+        hw = torch.from_numpy(inp.topk_weights).pin_memory()
+        hsc = torch.from_numpy(inp.x_scales).pin_memory() if inp.x_scales is not None else None
+        hout = torch.empty((w.num_tokens, w.hidden), dtype=torch.bfloat16).pin_memory()
+        dx = d.x.view(torch.uint8) if d.x.dtype == torch.uint8 else d.x.view(torch.int16)
+        eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            flush.zero_()
+            eev[i][0].record(stream)
+            dx.copy_(hx.view(dx.dtype).view(dx.shape), non_blocking=True)
+            d.topk_idx.copy_(hidx, non_blocking=True)
+            d.topk_weights.copy_(hw, non_blocking=True)
+            if hsc is not None:
+                d.x_scales.copy_(hsc, non_blocking=True)
+            path()
+            hout.copy_(step.buf.out.view(w.num_tokens, w.hidden), non_blocking=True)
+            eev[i][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = sum(a.elapsed_time(b) for a, b in eev)
+        h2d = hx.numel() * hx.element_size() + hidx.numel() * 4 + hw.numel() * 4 + \
+            (hsc.numel() * 4 if hsc is not None else 0)
+        d2h = hout.numel() * 2
+        e2e = {"value": None, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "local_ms_total": e2e_ms}
+        if not torch.equal(hout.view(torch.int16), step.buf.out.view(w.num_tokens, w.hidden).cpu().view(torch.int16)):
+            raise RuntimeError("end-to-end output differs from the device output")
+
+    clocks = sampler.stop()
+    status = step.error()
+    if status != B.MOE_OK:
+        raise RuntimeError(f"timed steps latched an error: {B.moe_status_string(status)}")
+
+    red_dev = dev
+    job = whole_job(w.num_tokens, sum(step_ms), K, world, red_dev)
+    if e2e is not None:
+        ej = whole_job(w.num_tokens, e2e.pop("local_ms_total"), K, world, red_dev)
+        e2e["value"] = ej["value"]
+        e2e["ms_per_step"] = ej["ms_per_step"]
+
+    if rank != 0:
+        return None
+
+    ab = w.algorithmic_bytes()
+    peak, peak_kind = measured_hbm_peak()
+    comb_s = kern_ms["combine"] / 1e3
+    achieved = ab["combine"] / comb_s / 1e9
+    traffic = profiled_traffic("moe_combine.cu", w.name)
+    kernels = {}
+    for name in ("layout", "dispatch", "combine"):
+        gbs = ab[name] / (kern_ms[name] / 1e3) / 1e9
+        kernels[name] = {"us": round(kern_ms[name] * 1e3, 3), "algorithmic_bytes": ab[name], "GBps": round(gbs, 1),
+                         "frac_of_measured_hbm": round(gbs / peak, 4)}
+    step_s = job["ms_per_step"] / 1e3
+    line = {
+        "metric": METRIC,
+        "value": round(job["value"], 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(job["ms_per_step"], 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp32",
+        "data": "synthetic",
+        "impl": "native",
+        "config": {
+            "workload": w.name,
+            "description": wl.DESCRIPTIONS[w.name],
+            "tokens_per_step_per_gpu": w.num_tokens,
+            "algorithmic_bytes_per_step": ab["total"],
+            "path": "layout (int32) -> dispatch (e4m3 rows + fp32 scales, byte copy) -> combine (bf16 in, fp32 "
+                    "accumulate, bf16 out); synthetic experts outside the timed region",
+            "l2": "flushed before every timed step (memset of 2x L2, outside the timed events)",
+            "parallelism": "replicas only: one independent EP group of 8 logical ranks per GPU",
+            "num_sms": args.num_sms,
+        },
+        "step_hbm": {"GBps": round(ab["total"] / step_s / 1e9, 1),
+                     "frac_of_8TBps": round(ab["total"] / step_s / 1e9 / NOMINAL_HBM_GBS, 4),
+                     "frac_of_measured": round(ab["total"] / step_s / 1e9 / peak, 4)},
+        "roofline": {"kernel": "combine_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": f"{peak_kind} (copy bandwidth)", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": ab["combine"]},
+        "kernels": kernels,
+        "e2e": e2e,
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world >= 1:
+        line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+    return line
+
+
+# --- the CPU oracle (baseline leg and reference arm) ---------------------------------
+
+def _oracle_sample_step(w, inp, sel):
+    """One oracle step over the selected tokens: layout (all tokens), dispatch and
+    combine of the selection; the synthetic experts run outside the timed part.
+    Returns seconds spent in layout + dispatch + combine."""
+    import oracle
+    dt = w.dtype_code
+    t0 = time.perf_counter()
+    counts, flags, tok_slot = oracle.layout(inp.topk_idx, w.num_experts, w.max_m)
+    slots = oracle.dispatch(inp.x, inp.x_scales, tok_slot, w.num_experts, w.max_m, dt, sel)
+    t1 = time.perf_counter()
+    y = oracle.expert_stub(slots, w.num_ranks, w.hidden, w.num_experts, w.max_m, dt)
+    t2 = time.perf_counter()
+    oracle.combine(tok_slot, inp.topk_weights, slots.slot_id, y, w.num_experts, w.max_m, sel)
+    t3 = time.perf_counter()
+    return (t1 - t0) + (t3 - t2)
+
+
+def _cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+def cpu_baseline(w, inp, seconds: float) -> dict:
+    """The oracle on the whole batch, repeated until about `seconds` of CPU work."""
+    import numpy as np
+    sel = np.arange(w.num_tokens, dtype=np.int64)
+    spent, reps = 0.0, 0
+    while reps < 1 or spent < seconds:
+        spent += _oracle_sample_step(w, inp, sel)
+        reps += 1
+        if reps >= 50:
+            break
+    return {"value": round(reps * w.num_tokens / spent, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} full {w.name} steps ({w.num_tokens} tokens each), single-threaded C oracle "
+                      f"(gcc -O2), synthetic experts excluded", "seconds": round(spent, 2),
+            "cpu": _cpu_model(), "host_cores_available": os.cpu_count()}
+
+
+def run_reference(args, rank, local_rank, world):
+    import numpy as np
+
+    from combine_moe_layout_gb300 import workloads as wl
+    if rank != 0:
+        return None
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w)
+    K, W = args.steps, args.warmup
+    # size each step's token sample so the whole run stays within ~2 minutes
+    pilot = np.arange(min(16, w.num_tokens), dtype=np.int64)
+    per_tok = _oracle_sample_step(w, inp, pilot) / pilot.size
+    budget = min(1.0, 120.0 / max(1, K + W))
+    n = int(max(1, min(w.num_tokens, budget / max(per_tok, 1e-9))))
+    cursor = 0
+
+    def next_sel():
+        nonlocal cursor
+        s = (np.arange(n, dtype=np.int64) + cursor) % w.num_tokens
+        cursor = (cursor + n) % w.num_tokens
+        return s
+
+    for _ in range(W):
+        _oracle_sample_step(w, inp, next_sel())
+    spent = sum(_oracle_sample_step(w, inp, next_sel()) for _ in range(K))
+    value = K * n / spent
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(spent / K * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "description": wl.DESCRIPTIONS[w.name],
+                   "sample": f"{n} of {w.num_tokens} tokens per step (layout over all tokens)"},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} tokens per step, {K} steps", "cpu": _cpu_model()},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=("native", "reference"), default="native")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--num-sms", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.steps is None:
+        args.steps = 2000 if args.impl == "native" else 20
+    if args.warmup is None:
+        args.warmup = 20 if args.impl == "native" else 3
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    rank, local_rank, world = dist_env()
+    if world != args.gpus and world > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE {world}")
+    line = (run_native if args.impl == "native" else run_reference)(args, rank, local_rank, world)
+    if line is not None and rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,31 @@
+"""GB300-native MoE expert-parallel token dispatch and combine on one GPU.
+
+The EP ranks are logical partitions of one device allocation. The work runs in
+libmoe_layout.so (hand-written CUDA for sm_103a behind the C ABI of
+include/moe_layout.h); this package holds its thin Python binding and the
+seeded workload generators.
+"""
+from ._binding import (  # noqa: F401
+    MOE_BF16,
+    MOE_EINVAL,
+    MOE_ECUDA,
+    MOE_ENOMEM,
+    MOE_EOVERFLOW,
+    MOE_ETIMEOUT,
+    MOE_FP8_E4M3,
+    MOE_OK,
+    MoeBuffers,
+    MoeDesc,
+    MoeError,
+    allocate_buffers,
+    library_path,
+    load,
+    moe_buffer_sizes,
+    moe_combine,
+    moe_dispatch,
+    moe_expert_stub,
+    moe_get_error,
+    moe_layout,
+    moe_reset,
+    moe_status_string,
+)

@@ -1,0 +1,179 @@
+"""Python binding of libmoe_layout.so: argument marshalling only.
+
+Every function has the name of the C entry point it calls (see
+include/moe_layout.h) and passes device pointers of torch tensors plus the
+current CUDA stream; all the work runs in the library's kernels. There is no
+fallback: if the library cannot be built or loaded, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _build
+
+MOE_OK, MOE_EINVAL, MOE_EOVERFLOW, MOE_ETIMEOUT, MOE_ECUDA, MOE_ENOMEM = 0, -1, -2, -3, -4, -5
+MOE_BF16, MOE_FP8_E4M3 = 0, 1
+
+
+class MoeDesc(ctypes.Structure):
+    _fields_ = [
+        ("num_ranks", ctypes.c_int32),
+        ("tokens_per_rank", ctypes.c_int32),
+        ("hidden", ctypes.c_int32),
+        ("num_experts", ctypes.c_int32),
+        ("topk", ctypes.c_int32),
+        ("max_m", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("num_sms", ctypes.c_int32),
+    ]
+
+    @classmethod
+    def of(cls, workload, num_sms: int = 0) -> "MoeDesc":
+        w = workload
+        return cls(w.num_ranks, w.tokens_per_rank, w.hidden, w.num_experts, w.topk, w.max_m, w.dtype_code, num_sms)
+
+
+class MoeSizes(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("recv_x", "recv_scales", "recv_meta", "counts", "flags", "tok_slot", "expert_out")]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {moe_status_string(status)} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Build (if stale) and open libmoe_layout.so; raises if that is impossible."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.build()
+    lib = ctypes.CDLL(path)
+    vp, st = ctypes.c_void_p, ctypes.c_int32
+    pdesc = ctypes.POINTER(MoeDesc)
+    lib.moe_buffer_sizes.argtypes = [pdesc, ctypes.POINTER(MoeSizes)]
+    lib.moe_layout.argtypes = [pdesc] + [vp] * 6
+    lib.moe_dispatch.argtypes = [pdesc] + [vp] * 9
+    lib.moe_expert_stub.argtypes = [pdesc] + [vp] * 6
+    lib.moe_combine.argtypes = [pdesc] + [vp] * 7
+    lib.moe_reset.argtypes = [pdesc] + [vp] * 3
+    lib.moe_get_error.argtypes = [vp, vp]
+    lib.moe_status_string.argtypes = [ctypes.c_int32]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    for name in ("moe_buffer_sizes", "moe_layout", "moe_dispatch", "moe_expert_stub", "moe_combine", "moe_reset",
+                 "moe_get_error"):
+        getattr(lib, name).restype = st
+    _lib = lib
+    return lib
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libmoe_layout takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("libmoe_layout takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, what: str):
+    if status != MOE_OK:
+        raise MoeError(status, what)
+
+
+def moe_status_string(status: int) -> str:
+    return load().moe_status_string(int(status)).decode()
+
+
+def moe_buffer_sizes(desc: MoeDesc) -> dict:
+    out = MoeSizes()
+    _check(load().moe_buffer_sizes(ctypes.byref(desc), ctypes.byref(out)), "moe_buffer_sizes")
+    return {name: int(getattr(out, name)) for name, _ in MoeSizes._fields_}
+
+
+def moe_layout(desc, topk_idx, counts, flags, tok_slot, err, stream=None):
+    _check(load().moe_layout(ctypes.byref(desc), _ptr(topk_idx), _ptr(counts), _ptr(flags), _ptr(tok_slot),
+                             _ptr(err), _stream(stream)), "moe_layout")
+
+
+def moe_dispatch(desc, x, x_scales, tok_slot, flags, recv_x, recv_scales, recv_meta, err, stream=None):
+    _check(load().moe_dispatch(ctypes.byref(desc), _ptr(x), _ptr(x_scales), _ptr(tok_slot), _ptr(flags),
+                               _ptr(recv_x), _ptr(recv_scales), _ptr(recv_meta), _ptr(err), _stream(stream)),
+           "moe_dispatch")
+
+
+def moe_expert_stub(desc, recv_x, recv_scales, counts, expert_out, err, stream=None):
+    _check(load().moe_expert_stub(ctypes.byref(desc), _ptr(recv_x), _ptr(recv_scales), _ptr(counts),
+                                  _ptr(expert_out), _ptr(err), _stream(stream)), "moe_expert_stub")
+
+
+def moe_combine(desc, expert_out, topk_weights, tok_slot, flags, out, err, stream=None):
+    _check(load().moe_combine(ctypes.byref(desc), _ptr(expert_out), _ptr(topk_weights), _ptr(tok_slot),
+                              _ptr(flags), _ptr(out), _ptr(err), _stream(stream)), "moe_combine")
+
+
+def moe_reset(desc, flags, err, stream=None):
+    _check(load().moe_reset(ctypes.byref(desc), _ptr(flags), _ptr(err), _stream(stream)), "moe_reset")
+
+
+def moe_get_error(err, stream=None) -> int:
+    """Synchronise, read and clear the device error word; returns its status code."""
+    return int(load().moe_get_error(_ptr(err), _stream(stream)))
+
+
+@dataclass
+class MoeBuffers:
+    """Device buffers of one step, sized by moe_buffer_sizes (allocated with torch)."""
+    counts: torch.Tensor
+    flags: torch.Tensor
+    tok_slot: torch.Tensor
+    recv_x: torch.Tensor
+    recv_scales: torch.Tensor | None
+    recv_meta: torch.Tensor
+    expert_out: torch.Tensor | None
+    out: torch.Tensor
+    err: torch.Tensor
+
+
+def allocate_buffers(desc: MoeDesc, device, with_expert_out: bool | None = None) -> MoeBuffers:
+    """Allocate every buffer of a step. expert_out is allocated for fp8 steps
+    (identity experts of bf16 steps read recv_x directly) unless overridden."""
+    sz = moe_buffer_sizes(desc)
+    R, T, H, E, k, M = desc.num_ranks, desc.tokens_per_rank, desc.hidden, desc.num_experts, desc.topk, desc.max_m
+    slots = E * R * M
+    fp8 = desc.dtype == MOE_FP8_E4M3
+    dev = torch.device(device)
+    recv_x = torch.empty(sz["recv_x"], dtype=torch.uint8, device=dev).view(slots, -1)
+    recv_scales = torch.empty((slots, H // 128), dtype=torch.float32, device=dev) if fp8 else None
+    if with_expert_out is None:
+        with_expert_out = fp8
+    expert_out = torch.empty((slots, H), dtype=torch.bfloat16, device=dev) if with_expert_out else None
+    return MoeBuffers(
+        counts=torch.zeros((E, R), dtype=torch.int32, device=dev),
+        flags=torch.zeros((E, R), dtype=torch.int64, device=dev),  # uint64 count+1 words
+        tok_slot=torch.empty((R, T, k), dtype=torch.int32, device=dev),
+        recv_x=recv_x,
+        recv_scales=recv_scales,
+        recv_meta=torch.empty((slots, 4), dtype=torch.int32, device=dev),
+        expert_out=expert_out,
+        out=torch.empty((R, T, H), dtype=torch.bfloat16, device=dev),
+        err=torch.zeros(1, dtype=torch.int32, device=dev),
+    )

@@ -1,0 +1,190 @@
+// Shared device and host helpers of libmoe_layout (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_layout.h"
+
+namespace moe {
+
+constexpr int kMaxTopk = 16;
+constexpr int kScaleBlock = 128;  // elements per fp32 scale of an fp8 row
+
+// Limits of the bounded waits, in nanoseconds of %globaltimer. A count+1 flag
+// is published by an earlier kernel in stream order, so a zero flag means the
+// layout step did not run: give up after 1 ms instead of hanging. A TMA
+// completion that never arrives would mean a fault: give up after 200 ms,
+// far longer than any copy takes.
+constexpr uint64_t kFlagWaitNs = 1000000ull;
+constexpr uint64_t kMbarWaitNs = 200000000ull;
+constexpr unsigned kFlagSleepNs = 128;
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// Error word: the first error a kernel finds wins.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void latch_error(int32_t *err, int32_t code) {
+  if (err != nullptr && *reinterpret_cast<volatile int32_t *>(err) == 0) atomicCAS(err, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// Flags: count + 1 signals, published with release and polled with acquire.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void store_release_u64(uint64_t *p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t load_acquire_u64(const uint64_t *p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait until *flag != 0; returns the flag (0 after giving up).
+__device__ __forceinline__ uint64_t wait_flag_nonzero(const uint64_t *flag) {
+  uint64_t v = load_acquire_u64(flag);
+  if (v != 0) return v;
+  const uint64_t t0 = global_timer_ns();
+  while (v == 0 && global_timer_ns() - t0 < kFlagWaitNs) {
+    __nanosleep(kFlagSleepNs);
+    v = load_acquire_u64(flag);
+  }
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier and bulk (non-tensor) TMA copies.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for phase `parity` of an mbarrier; false after giving up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < kMbarWaitNs)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// Global -> shared bulk copy completing on an mbarrier (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Shared -> global bulk copy tracked by bulk groups.
+__device__ __forceinline__ void bulk_store(void *gmem_dst, const void *smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
+               "r"(smem_addr(smem_src)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N committed bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until every committed bulk group has completed (writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Programmatic dependent launch: wait for the preceding kernel's results, and
+// allow the next kernel to start its prologue.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+struct Sizes {
+  int R, T, H, E, k, max_m, dtype, L;
+  int64_t nslots;     // E * R * max_m
+  int64_t ntok;       // R * T
+  int64_t row_bytes;  // 2H (bf16) or H (fp8)
+  int nsc;            // scales per row (H/128 for fp8, 0 for bf16)
+};
+
+// Independent restatement of the desc rules (see moe_layout.h).
+inline moe_status check_desc(const moe_desc *d, Sizes *s) {
+  if (d == nullptr) return MOE_EINVAL;
+  const int R = d->num_ranks, T = d->tokens_per_rank, H = d->hidden, E = d->num_experts, k = d->topk,
+            M = d->max_m;
+  if (R < 1 || T < 0 || H < 1 || E < 1 || k < 1 || M < 1) return MOE_EINVAL;
+  if (E % R != 0 || k > E || k > kMaxTopk || T > M) return MOE_EINVAL;
+  if (d->dtype == MOE_FP8_E4M3) {
+    if (H % kScaleBlock != 0) return MOE_EINVAL;
+  } else if (d->dtype == MOE_BF16) {
+    if (H % 8 != 0) return MOE_EINVAL;
+  } else {
+    return MOE_EINVAL;
+  }
+  if (d->num_sms < 0) return MOE_EINVAL;
+  if (static_cast<int64_t>(E) * R * M > INT32_MAX) return MOE_EINVAL;
+  if (static_cast<int64_t>(R) * T * k > INT32_MAX) return MOE_EINVAL;
+  if (s != nullptr) {
+    s->R = R;
+    s->T = T;
+    s->H = H;
+    s->E = E;
+    s->k = k;
+    s->max_m = M;
+    s->dtype = d->dtype;
+    s->L = E / R;
+    s->nslots = static_cast<int64_t>(E) * R * M;
+    s->ntok = static_cast<int64_t>(R) * T;
+    s->row_bytes = d->dtype == MOE_FP8_E4M3 ? H : 2 * static_cast<int64_t>(H);
+    s->nsc = d->dtype == MOE_FP8_E4M3 ? H / kScaleBlock : 0;
+  }
+  return MOE_OK;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+inline moe_status launch_status() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ECUDA; }
+
+// SM count of the current device (queried once per device).
+int sm_count();
+
+}  // namespace moe

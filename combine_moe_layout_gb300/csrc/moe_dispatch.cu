@@ -1,0 +1,225 @@
+// Dispatch (K2): copy every token row, with its fp32 block scales and a
+// 16-byte header, into its k fixed slots.
+//
+// Perplexity, "Efficient and portable mixture-of-experts communication",
+// section "Dispatch": activations, scales and the token's index on its own rank
+// are packed and sent to each chosen expert; the receiver keeps (source rank,
+// expert, token) for combine. "NVSHMEM and DeepEP: GPU-initiated
+// communication": FP8 rows with one fp32 scale per 128 elements, written into
+// the receiver's fixed slots. On one GPU a "put" into a peer's slot is a store
+// into that rank's partition of the one allocation.
+//
+// Design: a work unit is (row, piece of at most 16 KiB). Each CTA is one warp
+// and owns units blockIdx.x, blockIdx.x + gridDim.x, ... Lane 0 streams the
+// unit bytes global -> shared with bulk TMA loads (S stages, one mbarrier
+// each), and writes each staged piece to its k slots with bulk TMA stores
+// (shared -> global, tracked by bulk groups); a stage is refilled once its
+// stores have finished reading it. While a load is in flight, the other lanes
+// read the unit's k slot ids, wait (bounded) on the count+1 flags of the
+// destination regions, and write the headers and scales with plain stores.
+// The grid is sized to the resident CTA count, so every load of a small batch
+// is issued at once.
+#include "moe_common.cuh"
+
+namespace moe {
+
+constexpr uint32_t kPieceMax = 16384;       // bytes staged per unit
+constexpr uint32_t kStageBudget = 32768;    // shared bytes of staging per CTA
+constexpr int kMaxStages = 8;
+
+struct DispatchArgs {
+  const uint8_t *x;
+  const float *x_scales;
+  const int32_t *tok_slot;
+  const uint64_t *flags;
+  uint8_t *recv_x;
+  float *recv_scales;
+  int4 *recv_meta;
+  int32_t *err;
+  int R, T, k, max_m, nsc, stages, pieces;
+  uint32_t row_bytes, piece_bytes;
+  int64_t nslots, nunits;
+};
+
+__device__ __forceinline__ void issue_unit_load(const DispatchArgs &a, uint8_t *stage, uint64_t *bar, int64_t unit) {
+  const int64_t row = unit / a.pieces;
+  const uint32_t off = static_cast<uint32_t>(unit % a.pieces) * a.piece_bytes;
+  const uint32_t bytes = min(a.piece_bytes, a.row_bytes - off);
+  mbar_arrive_expect_tx(bar, bytes);
+  bulk_load(stage, a.x + row * a.row_bytes + off, bytes, bar);
+}
+
+__global__ void __launch_bounds__(32) dispatch_kernel(DispatchArgs a) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ uint64_t full[kMaxStages];
+  __shared__ int32_t dst[kMaxTopk];
+  __shared__ int aborted;
+
+  const int lane = threadIdx.x;
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+  const int64_t n_mine = first < a.nunits ? (a.nunits - 1 - first) / stride + 1 : 0;
+  const int S = a.stages;
+
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+    aborted = 0;
+  }
+  __syncwarp();
+  grid_dependency_wait();
+
+  if (lane == 0)
+    for (int64_t i = 0; i < n_mine && i < S; ++i)
+      issue_unit_load(a, dsm + static_cast<size_t>(i) * a.piece_bytes, &full[i], first + i * stride);
+
+  int64_t i = 0;
+  for (; i < n_mine; ++i) {
+    const int s = static_cast<int>(i % S);
+    const uint32_t parity = static_cast<uint32_t>((i / S) & 1);
+    const int64_t unit = first + i * stride;
+    const int64_t row = unit / a.pieces;
+    const int piece = static_cast<int>(unit % a.pieces);
+    const uint32_t off = static_cast<uint32_t>(piece) * a.piece_bytes;
+    const uint32_t bytes = min(a.piece_bytes, a.row_bytes - off);
+
+    // destinations of this row, checked against the flags of their regions
+    if (lane < a.k) {
+      int32_t slot = a.tok_slot[row * a.k + lane];
+      if (slot >= a.nslots) {
+        latch_error(a.err, MOE_EINVAL);
+        slot = -1;
+      } else if (slot >= 0) {
+        if (wait_flag_nonzero(a.flags + slot / a.max_m) == 0) {
+          latch_error(a.err, MOE_ETIMEOUT);
+          slot = -1;
+        }
+      }
+      dst[lane] = slot;
+    }
+    __syncwarp();
+
+    if (piece == 0) {
+      const int src = static_cast<int>(row / a.T), t = static_cast<int>(row % a.T);
+      if (lane < a.k && dst[lane] >= 0) {
+        const int32_t slot = dst[lane];
+        a.recv_meta[slot] = make_int4(src, t, (slot / a.max_m) / a.R, lane);
+      }
+      if (a.nsc > 0) {
+        const float *sc = a.x_scales + row * a.nsc;
+        for (int q = lane; q < a.k * a.nsc; q += 32) {
+          const int j = q / a.nsc, c = q - j * a.nsc;
+          const int32_t slot = dst[j];
+          if (slot >= 0) a.recv_scales[static_cast<int64_t>(slot) * a.nsc + c] = __ldg(sc + c);
+        }
+      }
+    }
+
+    if (lane == 0) {
+      uint8_t *stage = dsm + static_cast<size_t>(s) * a.piece_bytes;
+      if (!mbar_wait_bounded(&full[s], parity)) {
+        latch_error(a.err, MOE_ETIMEOUT);
+        aborted = 1;
+      } else {
+        for (int j = 0; j < a.k; ++j) {
+          const int32_t slot = dst[j];
+          if (slot >= 0) bulk_store(a.recv_x + static_cast<int64_t>(slot) * a.row_bytes + off, stage, bytes);
+        }
+        bulk_commit();
+        // refill the stage of the previous unit once its stores have read it
+        const int64_t next = i - 1 + S;
+        if (i >= 1 && next < n_mine) {
+          bulk_wait_read<1>();
+          const int ps = static_cast<int>((i - 1) % S);
+          issue_unit_load(a, dsm + static_cast<size_t>(ps) * a.piece_bytes, &full[ps], first + next * stride);
+        }
+      }
+    }
+    __syncwarp();
+    if (aborted) break;
+  }
+
+  if (lane == 0) {
+    if (aborted) {
+      // Drain the loads still in flight (bounded) before the CTA releases its
+      // shared memory: units i .. i+S-2 were issued (the refill of unit i-1+S
+      // had not happened yet).
+      const int64_t issued = n_mine < i + S - 1 ? n_mine : i + S - 1;
+      for (int64_t u = i; u < issued; ++u)
+        mbar_wait_bounded(&full[u % S], static_cast<uint32_t>((u / S) & 1));
+    }
+    bulk_wait_all();
+  }
+  __syncwarp();
+  grid_dependents_launch();
+}
+
+moe_status launch_dispatch(const Sizes &s, const void *x, const float *x_scales, const int32_t *tok_slot,
+                           const uint64_t *flags, void *recv_x, float *recv_scales, int32_t *recv_meta,
+                           int32_t *err, int num_sms, cudaStream_t stream) {
+  DispatchArgs a{};
+  a.x = static_cast<const uint8_t *>(x);
+  a.x_scales = x_scales;
+  a.tok_slot = tok_slot;
+  a.flags = flags;
+  a.recv_x = static_cast<uint8_t *>(recv_x);
+  a.recv_scales = recv_scales;
+  a.recv_meta = reinterpret_cast<int4 *>(recv_meta);
+  a.err = err;
+  a.R = s.R;
+  a.T = s.T;
+  a.k = s.k;
+  a.max_m = s.max_m;
+  a.nsc = s.nsc;
+  a.row_bytes = static_cast<uint32_t>(s.row_bytes);
+  a.piece_bytes = a.row_bytes < kPieceMax ? a.row_bytes : kPieceMax;
+  a.pieces = static_cast<int>((a.row_bytes + a.piece_bytes - 1) / a.piece_bytes);
+  a.nslots = s.nslots;
+  a.nunits = s.ntok * a.pieces;
+  int stages = static_cast<int>(kStageBudget / a.piece_bytes);
+  a.stages = stages < 2 ? 2 : (stages > kMaxStages ? kMaxStages : stages);
+  if (a.nunits == 0) return MOE_OK;
+
+  const size_t smem = static_cast<size_t>(a.stages) * a.piece_bytes;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel, 32, smem) != cudaSuccess)
+    return MOE_ECUDA;
+  if (per_sm < 1) per_sm = 1;
+  const int sms = num_sms > 0 && num_sms < sm_count() ? num_sms : sm_count();
+  int64_t grid = static_cast<int64_t>(sms) * per_sm;
+  if (grid > a.nunits) grid = a.nunits;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, dispatch_kernel, a) != cudaSuccess) return MOE_ECUDA;
+  return launch_status();
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status moe_dispatch(const moe_desc *desc, const void *x, const float *x_scales,
+                                   const int32_t *tok_slot, const uint64_t *flags, void *recv_x,
+                                   float *recv_scales, int32_t *recv_meta, int32_t *err, void *stream) {
+  Sizes s;
+  moe_status st = check_desc(desc, &s);
+  if (st != MOE_OK) return st;
+  if (flags == nullptr || err == nullptr || recv_x == nullptr || recv_meta == nullptr) return MOE_EINVAL;
+  if (s.ntok > 0 && (x == nullptr || tok_slot == nullptr)) return MOE_EINVAL;
+  if (s.dtype == MOE_FP8_E4M3) {
+    if (recv_scales == nullptr || (s.ntok > 0 && x_scales == nullptr)) return MOE_EINVAL;
+    if (!aligned4(x_scales) || !aligned4(recv_scales)) return MOE_EINVAL;
+  }
+  if (!aligned16(x) || !aligned16(recv_x) || !aligned16(recv_meta) || !aligned4(tok_slot) || !aligned4(err))
+    return MOE_EINVAL;
+  return launch_dispatch(s, x, x_scales, tok_slot, flags, recv_x, recv_scales, recv_meta, err, desc->num_sms,
+                         static_cast<cudaStream_t>(stream));
+}

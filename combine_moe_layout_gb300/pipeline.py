@@ -1,0 +1,84 @@
+"""One dispatch/combine step through the C ABI, with torch for device memory.
+
+``MoeStep`` owns the device buffers of one problem size and runs
+layout -> dispatch -> experts -> combine on a stream. The experts are the
+synthetic ones of the workloads: identity for bf16 steps (combine reads the
+receive buffer itself) and ``moe_expert_stub`` for fp8 steps.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import _binding as B
+
+
+@dataclass
+class DeviceInputs:
+    topk_idx: torch.Tensor      # [R][T][k] int32
+    topk_weights: torch.Tensor  # [R][T][k] float32
+    x: torch.Tensor             # [R][T][H] uint8 (fp8 codes) or bfloat16
+    x_scales: torch.Tensor | None
+
+
+def to_device(inputs, device, pin: bool = False) -> DeviceInputs:
+    """Copy generated numpy inputs to the device (bf16 bits are reinterpreted, not converted)."""
+    def t(a):
+        ht = torch.from_numpy(np.ascontiguousarray(a))
+        if pin:
+            ht = ht.pin_memory()
+        return ht.to(device, non_blocking=pin)
+
+    x = t(inputs.x)
+    if x.dtype == torch.uint16:
+        x = x.view(torch.bfloat16)
+    elif x.dtype != torch.uint8:
+        raise ValueError("x must hold uint16 bf16 bits or uint8 e4m3 codes")
+    return DeviceInputs(t(inputs.topk_idx), t(inputs.topk_weights), x,
+                        None if inputs.x_scales is None else t(inputs.x_scales))
+
+
+class MoeStep:
+    def __init__(self, workload, device="cuda", num_sms: int = 0, buffers: B.MoeBuffers | None = None):
+        self.w = workload
+        self.desc = B.MoeDesc.of(workload, num_sms)
+        self.fp8 = workload.dtype == "fp8"
+        self.device = torch.device(device)
+        self.buf = buffers if buffers is not None else B.allocate_buffers(self.desc, self.device)
+        self.slots = workload.num_experts * workload.num_ranks * workload.max_m
+        if self.buf.expert_out is not None:
+            self.y = self.buf.expert_out
+        else:  # identity experts: combine reads the dispatched rows themselves
+            self.y = self.buf.recv_x.view(torch.bfloat16).view(self.slots, workload.hidden)
+
+    def reset(self, stream=None):
+        B.moe_reset(self.desc, self.buf.flags, self.buf.err, stream)
+
+    def layout(self, d: DeviceInputs, stream=None):
+        b = self.buf
+        B.moe_layout(self.desc, d.topk_idx, b.counts, b.flags, b.tok_slot, b.err, stream)
+
+    def dispatch(self, d: DeviceInputs, stream=None):
+        b = self.buf
+        B.moe_dispatch(self.desc, d.x, d.x_scales, b.tok_slot, b.flags, b.recv_x, b.recv_scales, b.recv_meta, b.err,
+                       stream)
+
+    def experts(self, stream=None):
+        if self.fp8:
+            b = self.buf
+            B.moe_expert_stub(self.desc, b.recv_x, b.recv_scales, b.counts, b.expert_out, b.err, stream)
+
+    def combine(self, d: DeviceInputs, stream=None):
+        b = self.buf
+        B.moe_combine(self.desc, self.y, d.topk_weights, b.tok_slot, b.flags, b.out, b.err, stream)
+
+    def run(self, d: DeviceInputs, stream=None):
+        self.layout(d, stream)
+        self.dispatch(d, stream)
+        self.experts(stream)
+        self.combine(d, stream)
+
+    def error(self, stream=None) -> int:
+        return B.moe_get_error(self.buf.err, stream)

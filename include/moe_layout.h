@@ -1,0 +1,164 @@
+/*
+ * moe_layout.h - C ABI of libmoe_layout.so: MoE expert-parallel token dispatch
+ * and combine on one GPU, with the EP ranks as logical partitions of one
+ * device allocation.
+ *
+ * Sources, cited by page title and section:
+ *   "How GPUs Talk to Each Other During LLM Inference", section 7 "Expert
+ *     Parallelism": dispatch sends each token's hidden state to the ranks of its
+ *     top-k experts, grouped by expert; combine weights each expert output by
+ *     its router score and sums the k outputs at the token's home rank.
+ *   Perplexity, "Efficient and portable mixture-of-experts communication",
+ *     sections "Portable kernels", "Dispatch", "Combine": count + 1 signals,
+ *     private per-(expert, sender) receive regions sized by max_m, token index
+ *     kept for combine, weighted sum at the receiver into a caller tensor.
+ *   "NVSHMEM and DeepEP: GPU-initiated communication", sections
+ *     "High-throughput mode" (FP8 dispatch with one fp32 scale per 128
+ *     elements, BF16 combine) and "Low-latency mode: fixed slots, no CPU sync"
+ *     (max_m slots per local expert and source rank; no host sync; static
+ *     shapes).
+ *
+ * Conventions for every call:
+ *   - Sizes: R = num_ranks logical EP ranks, T = tokens_per_rank, H = hidden,
+ *     E = num_experts, L = E / R local experts, k = topk, max_m = slots per
+ *     (expert, source rank). Expert e lives on rank e / L.
+ *   - Slot ids: region r = e * R + src, slot s = r * max_m + pos. Rank d owns
+ *     the contiguous slot range [d*L*R*max_m, (d+1)*L*R*max_m), i.e. the
+ *     receiver's [local expert][source rank][max_m] buffer, ranks concatenated.
+ *   - Pointers are device pointers unless stated; the caller allocates every
+ *     buffer (moe_buffer_sizes gives the sizes) and the library allocates
+ *     nothing and keeps no state between calls.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *     asynchronous on it and never synchronise with the host, except
+ *     moe_get_error.
+ *   - The return value reports host-side validation (MOE_EINVAL) and launch
+ *     failures (MOE_ECUDA). Errors found by a kernel are latched into the
+ *     caller's device word `err` (int32, first error wins) and read with
+ *     moe_get_error. Kernels never trap: they skip the offending access.
+ *   - One step is moe_layout -> moe_dispatch -> (the caller's experts) ->
+ *     moe_combine, in stream order on one stream.
+ */
+#ifndef MOE_LAYOUT_H
+#define MOE_LAYOUT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_EINVAL = -1,    /* invalid sizes, pointers or routing */
+  MOE_EOVERFLOW = -2, /* more tokens for an (expert, source) than max_m slots */
+  MOE_ETIMEOUT = -3,  /* a bounded wait on a count+1 flag gave up */
+  MOE_ECUDA = -4,     /* a CUDA runtime call or launch failed */
+  MOE_ENOMEM = -5     /* reserved for callers that size buffers from free memory */
+} moe_status;
+
+typedef enum {
+  MOE_BF16 = 0,     /* rows of H bfloat16 */
+  MOE_FP8_E4M3 = 1  /* rows of H e4m3 bytes + H/128 fp32 scales */
+} moe_dtype;
+
+/* The problem statement: tokens, routing, EP ranks and the per-rank bound. */
+typedef struct {
+  int32_t num_ranks;       /* R >= 1 */
+  int32_t tokens_per_rank; /* 0 <= T <= max_m */
+  int32_t hidden;          /* H; multiple of 8 (bf16) or of 128 (fp8) */
+  int32_t num_experts;     /* E, a multiple of R */
+  int32_t topk;            /* 1 <= k <= min(E, 16) */
+  int32_t max_m;           /* slots per (expert, source rank), >= 1 */
+  int32_t dtype;           /* moe_dtype of the dispatched rows */
+  int32_t num_sms;         /* SMs the dispatch kernel may occupy; 0 = all */
+} moe_desc;
+
+/* Bytes of each buffer of one step, for all R logical ranks together. */
+typedef struct {
+  size_t recv_x;      /* [E][R][max_m] rows (2H bytes bf16, H bytes fp8) */
+  size_t recv_scales; /* [E][R][max_m][H/128] float (0 for bf16) */
+  size_t recv_meta;   /* [E][R][max_m] int32x4 header per slot */
+  size_t counts;      /* [E][R] int32 */
+  size_t flags;       /* [E][R] uint64 */
+  size_t tok_slot;    /* [R][T][k] int32 */
+  size_t expert_out;  /* [E][R][max_m][H] bfloat16 */
+} moe_sizes;
+
+/* Sizes of every buffer. Host-only; no GPU needed. Per slot a receiver holds a
+ * row, its scales and a 16-byte header: the per-slot message of the
+ * low-latency receive-buffer estimate ("NVSHMEM and DeepEP", low-latency
+ * section: hidden + hidden/128*4 + 16 bytes). Returns MOE_EINVAL for an
+ * invalid desc or NULL pointers. */
+moe_status moe_buffer_sizes(const moe_desc *desc, moe_sizes *out);
+
+/* Layout (the counting side of dispatch; Perplexity, "Dispatch"). For every
+ * source rank src and expert e: counts[e*R+src] = number of tokens of src that
+ * chose e; flags[e*R+src] = counts + 1 (the 0 -> non-zero change means "count
+ * arrived"); tok_slot[(src*T+t)*k+j] = the fixed slot of choice j of token t,
+ * with pos = number of earlier tokens of src that chose the same expert (token
+ * order, so positions are deterministic).
+ *   topk_idx [R][T][k] int32 in [0, E), distinct within a token (read).
+ *   counts [E][R] int32, flags [E][R] uint64, tok_slot [R][T][k] int32 (written).
+ *   err: device int32 error word.
+ * Device errors: an expert id outside [0, E) or repeated within a token ->
+ * MOE_EINVAL and tok_slot = -1 for that entry; pos >= max_m -> MOE_EOVERFLOW and
+ * tok_slot = -1. */
+moe_status moe_layout(const moe_desc *desc, const int32_t *topk_idx, int32_t *counts, uint64_t *flags,
+                      int32_t *tok_slot, int32_t *err, void *stream);
+
+/* Dispatch (pack and scatter; Perplexity, "Dispatch"; "NVSHMEM and DeepEP",
+ * low-latency section). Waits, bounded, until the count+1 flag of each
+ * destination region is non-zero, then copies row (src, t) and its scales into
+ * each of its k slots and writes the slot header {src, t, e, j}.
+ *   x [R][T] rows: H bf16 (2H bytes) or H e4m3 bytes; 16-byte aligned (read).
+ *   x_scales [R][T][H/128] float (fp8 only; NULL for bf16) (read).
+ *   tok_slot, flags: from moe_layout (read).
+ *   recv_x [E][R][max_m] rows, 16-byte aligned; recv_scales [E][R][max_m][H/128]
+ *   (fp8 only; NULL for bf16); recv_meta [E][R][max_m][4] int32, 16-byte
+ *   aligned (written; only slots pos < count are touched).
+ * Device errors: a flag still zero after the bounded wait -> MOE_ETIMEOUT;
+ * tok_slot out of range -> MOE_EINVAL; the affected copies are skipped. */
+moe_status moe_dispatch(const moe_desc *desc, const void *x, const float *x_scales, const int32_t *tok_slot,
+                        const uint64_t *flags, void *recv_x, float *recv_scales, int32_t *recv_meta,
+                        int32_t *err, void *stream);
+
+/* Synthetic experts for tests and benchmarks (not part of the pages' method):
+ * for every filled slot (pos < counts) of an fp8 step,
+ * expert_out = bf16_rne(e4m3(q) * scale * (1 + e/256)), the product taken
+ * exactly and rounded once. bf16 steps use identity experts: pass recv_x as
+ * expert_out to moe_combine instead (this call returns MOE_EINVAL for bf16).
+ *   recv_x, recv_scales, counts (read); expert_out [E][R][max_m][H] bf16,
+ *   16-byte aligned (written for filled slots only). */
+moe_status moe_expert_stub(const moe_desc *desc, const void *recv_x, const float *recv_scales,
+                           const int32_t *counts, uint16_t *expert_out, int32_t *err, void *stream);
+
+/* Combine (Perplexity, "Combine"; "How GPUs Talk", section 7). For every token:
+ * out[src][t][h] = bf16_rne( sum_{j<k} w[src][t][j] * Y[tok_slot[src][t][j]][h] ),
+ * the products and sum in fp32, choices in order j = 0..k-1, weights applied at
+ * the receiver. Then clears flags to zero so the next step's layout signals
+ * afresh (the dispatch -> combine barrier becomes stream order).
+ *   expert_out Y [E][R][max_m][H] bf16, 16-byte aligned (read at slots only).
+ *   topk_weights [R][T][k] float; tok_slot [R][T][k] (read).
+ *   flags [E][R] (zeroed). out [R][T][H] bf16, 16-byte aligned (written).
+ * Device errors: tok_slot >= E*R*max_m -> MOE_EINVAL (the term is skipped);
+ * tok_slot < 0 (an entry layout rejected) contributes nothing. */
+moe_status moe_combine(const moe_desc *desc, const uint16_t *expert_out, const float *topk_weights,
+                       const int32_t *tok_slot, uint64_t *flags, uint16_t *out, int32_t *err, void *stream);
+
+/* Clear flags [E][R] and the error word (for the first step, or after an
+ * aborted one). */
+moe_status moe_reset(const moe_desc *desc, uint64_t *flags, int32_t *err, void *stream);
+
+/* Synchronise `stream`, read the device error word, clear it, and return its
+ * value (MOE_OK if no kernel latched an error). Host-synchronising. */
+moe_status moe_get_error(int32_t *err, void *stream);
+
+/* Static description of a status code. */
+const char *moe_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LAYOUT_H */

@@ -1,0 +1,281 @@
+"""GPU path vs the CPU oracle, through the C ABI.
+
+Dispatch must agree bit-exactly (slot contents, scales, counts, headers),
+compared per (source rank, token); combine within 2^-7 relative per element,
+with exact zeros. Small configs are compared in full; the large ones in full
+for layout, on a seeded sample of tokens for dispatch and combine, and through
+properties that hold at any size (identity experts return the input; scaling
+experts follow their closed form) for every token.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_moe_layout_gb300 import _binding as B
+from combine_moe_layout_gb300 import pipeline as P
+from combine_moe_layout_gb300 import workloads as wl
+from gpu_common import (TOL, assert_combine_close, check_dispatch, check_layout, check_region_sets,
+                        check_touched_slots_gpu, free_gpu, require_gpu, run_step)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    require_gpu()
+    yield
+    free_gpu()
+
+
+def _sample(w, n, seed=7):
+    N = w.num_tokens
+    if n >= N:
+        return np.arange(N, dtype=np.int64)
+    rng = np.random.default_rng(seed)
+    s = rng.choice(N, size=n - 2, replace=False)
+    return np.unique(np.concatenate([s, [0, N - 1]])).astype(np.int64)
+
+
+def _full_parity(w, inp, num_sms=0, region_sets=True):
+    ref = oracle.run(w, inp)
+    step, d, flags, err, _ = run_step(w, inp, num_sms=num_sms)
+    assert err == B.MOE_OK, B.moe_status_string(err)
+    ts = check_layout(step, flags, ref, w)
+    check_dispatch(step, w, ts, ref)
+    if region_sets:
+        check_region_sets(step, w, ts, ref)
+    else:
+        check_touched_slots_gpu(step, w, ref.counts)
+    out = step.buf.out.view(torch.int16).cpu().numpy().view(np.uint16).reshape(w.num_tokens, w.hidden)
+    assert_combine_close(out, ref.out)
+    assert not step.buf.flags.any().item(), "combine must clear the count+1 flags"
+    return step, d, ref, out
+
+
+def test_tiny():
+    w = wl.WORKLOADS["tiny"]
+    inp = wl.make_inputs(w)
+    step, d, ref, out = _full_parity(w, inp)
+    # identity experts, renormalised weights: combine returns the input
+    assert np.array_equal(out, inp.x.reshape(w.num_tokens, w.hidden))
+
+
+def test_ds_decode():
+    w = wl.WORKLOADS["ds_decode"]
+    _full_parity(w, wl.make_inputs(w), region_sets=False)
+
+
+def test_skewed():
+    w = wl.WORKLOADS["skewed"]
+    inp = wl.make_inputs(w)
+    step, d, ref, out = _full_parity(w, inp, region_sets=False)
+    assert np.array_equal(out, inp.x.reshape(w.num_tokens, w.hidden))
+    # the hot expert fills nearly all of rank 0's slots for it
+    assert ref.counts[0].max() > 0.9 * w.tokens_per_rank
+
+
+def _large_parity(w, n_sample):
+    inp = wl.make_inputs(w)
+    sel = _sample(w, n_sample)
+    counts, flags, tok_slot = oracle.layout(inp.topk_idx, w.num_experts, w.max_m)
+    dt = w.dtype_code
+    slots = oracle.dispatch(inp.x, inp.x_scales, tok_slot, w.num_experts, w.max_m, dt, sel)
+    y = oracle.expert_stub(slots, w.num_ranks, w.hidden, w.num_experts, w.max_m, dt)
+    out_ref = oracle.combine(tok_slot, inp.topk_weights, slots.slot_id, y, w.num_experts, w.max_m, sel)
+    ref = oracle.OracleResult(counts, flags, tok_slot, slots, y, out_ref, sel)
+    step, d, fl, err, _ = run_step(w, inp)
+    assert err == B.MOE_OK, B.moe_status_string(err)
+    ts = check_layout(step, fl, ref, w)
+    check_dispatch(step, w, ts, ref)
+    check_touched_slots_gpu(step, w, counts)
+    out_t = step.buf.out.view(w.num_tokens, w.hidden)
+    got = out_t.index_select(0, torch.from_numpy(sel).cuda()).view(torch.int16).cpu().numpy().view(np.uint16)
+    assert_combine_close(got, out_ref)
+    return step, d, inp
+
+
+def test_mixtral():
+    w = wl.WORKLOADS["mixtral"]
+    step, d, inp = _large_parity(w, 2048)
+    # every token: identity experts with renormalised weights give back x exactly
+    assert torch.equal(step.buf.out.view(torch.int16), d.x.view(torch.int16))
+
+
+def _scaled_closed_form_all_tokens(step, d, w, chunk=2048):
+    """out ~= x_deq * sum_j w_j (1 + e_j/256) within 2^-7 for every token (on the device)."""
+    out = step.buf.out.view(w.num_tokens, w.hidden)
+    x = d.x.view(w.num_tokens, w.hidden)
+    sc = d.x_scales.view(w.num_tokens, -1)
+    c = (d.topk_weights.double() * (1 + d.topk_idx.double() / 256)).sum(-1).view(-1)
+    for t0 in range(0, w.num_tokens, chunk):
+        t1 = min(w.num_tokens, t0 + chunk)
+        deq = x[t0:t1].view(torch.float8_e4m3fn).float().double() * sc[t0:t1].double().repeat_interleave(128, dim=1)
+        ref = deq * c[t0:t1, None]
+        got = out[t0:t1].double()
+        assert bool(((got - ref).abs() <= TOL * ref.abs()).all())
+        assert bool((got[ref == 0] == 0).all())
+
+
+def test_ds_decode_closed_form():
+    w = wl.WORKLOADS["ds_decode"]
+    inp = wl.make_inputs(w)
+    step, d, flags, err, _ = run_step(w, inp)
+    assert err == B.MOE_OK
+    _scaled_closed_form_all_tokens(step, d, w)
+
+
+def test_ds_prefill():
+    w = wl.WORKLOADS["ds_prefill"]
+    free = torch.cuda.mem_get_info()[0]
+    need = sum(B.moe_buffer_sizes(B.MoeDesc.of(w)).values()) + (2 << 30)
+    assert free > need, f"ds_prefill needs {need / 2**30:.1f} GiB of device memory, {free / 2**30:.1f} free"
+    step, d, inp = _large_parity(w, 512)
+    _scaled_closed_form_all_tokens(step, d, w)
+    # group-limited routing: each token reaches at most 4 logical ranks
+    ranks = (d.topk_idx.long() // w.local_experts)
+    per_tok = torch.stack([(ranks == r).any(-1) for r in range(w.num_ranks)], -1).sum(-1)
+    assert int(per_tok.max()) <= 4
+
+
+# --- edge cases ------------------------------------------------------------------
+
+EDGE = {
+    "minimal": dict(num_ranks=1, tokens_per_rank=1, hidden=8, num_experts=1, topk=1, max_m=1),
+    "ragged_chunks_k3": dict(num_ranks=3, tokens_per_rank=300, hidden=256, num_experts=12, topk=3, max_m=300),
+    "k16_fp8_one_scale": dict(num_ranks=2, tokens_per_rank=130, hidden=128, num_experts=32, topk=16, max_m=200,
+                              dtype="fp8", expert="scale", x_dist="normal"),
+    "two_pieces_per_row": dict(num_ranks=4, tokens_per_rank=64, hidden=16384, num_experts=8, topk=2, max_m=64,
+                               x_dist="normal"),
+    "decode_plus_one": dict(num_ranks=8, tokens_per_rank=129, hidden=7168, num_experts=256, topk=8, max_m=129,
+                            dtype="fp8", expert="scale", x_dist="normal", renormalize=False),
+    "slots_exceed_tokens": dict(num_ranks=2, tokens_per_rank=20, hidden=64, num_experts=4, topk=4, max_m=33),
+    "k6_bf16": dict(num_ranks=4, tokens_per_rank=77, hidden=1024, num_experts=16, topk=6, max_m=80),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+def test_edge_shapes(name):
+    w = wl.custom(name, **EDGE[name])
+    _full_parity(w, wl.make_inputs(w, seed=3), region_sets=w.num_experts * w.num_ranks * w.max_m * w.row_bytes < (1 << 28))
+
+
+@pytest.mark.parametrize("num_sms", [1, 3])
+def test_few_sms_deep_pipeline(num_sms):
+    """With one or three SMs every dispatch CTA streams many rows through its stages."""
+    w = wl.custom("deep", num_ranks=4, tokens_per_rank=200, hidden=2048, num_experts=16, topk=4, max_m=200,
+                  x_dist="normal")
+    _full_parity(w, wl.make_inputs(w, seed=5), num_sms=num_sms, region_sets=False)
+
+
+def test_empty_batch():
+    w = wl.custom("empty", num_ranks=2, tokens_per_rank=0, hidden=128, num_experts=4, topk=2, max_m=4)
+    inp = wl.make_inputs(w)
+    step, d, flags, err, guards = run_step(w, inp, guards=True)
+    assert err == B.MOE_OK
+    assert not step.buf.counts.any().item()
+    assert bool((flags == 1).all()), "an empty batch still signals count + 1 = 1"
+    assert all(g.guards_intact() for g in guards)
+
+
+def test_repeated_steps_reuse_buffers():
+    """Combine clears the flags, so the same buffers serve the next step."""
+    w = wl.custom("rep", num_ranks=4, tokens_per_rank=50, hidden=512, num_experts=16, topk=4, max_m=64,
+                  dtype="fp8", expert="scale", x_dist="normal")
+    step = P.MoeStep(w, "cuda:0")
+    step.reset()
+    for seed in (1, 2, 3):
+        inp = wl.make_inputs(w, seed=seed)
+        ref = oracle.run(w, inp)
+        d = P.to_device(inp, "cuda:0")
+        step.run(d)
+        assert step.error() == B.MOE_OK
+        out = step.buf.out.view(torch.int16).cpu().numpy().view(np.uint16).reshape(w.num_tokens, w.hidden)
+        assert_combine_close(out, ref.out)
+        assert np.array_equal(step.buf.tok_slot.cpu().numpy(), ref.tok_slot)
+
+
+def test_layout_is_deterministic():
+    w = wl.WORKLOADS["ds_decode"]
+    inp = wl.make_inputs(w)
+    step = P.MoeStep(w, "cuda:0")
+    d = P.to_device(inp, "cuda:0")
+    step.reset()
+    seen = []
+    for _ in range(3):
+        step.layout(d)
+        seen.append(step.buf.tok_slot.clone())
+        step.reset()
+    assert all(torch.equal(seen[0], s) for s in seen[1:])
+
+
+# --- error paths (no fault, no trap: the kernels latch a status and skip) ----------
+
+def _guarded_run(w, topk_idx, stages=("layout", "dispatch", "experts", "combine"), reset_before_dispatch=False):
+    inp = wl.make_inputs(w)
+    inp.topk_idx[...] = topk_idx
+    step, d, flags, err, guards = None, None, None, None, None
+    desc = B.MoeDesc.of(w)
+    from gpu_common import guarded_buffers
+    bufs, guards = guarded_buffers(desc, "cuda:0")
+    step = P.MoeStep(w, "cuda:0", buffers=bufs)
+    d = P.to_device(inp, "cuda:0")
+    step.reset()
+    step.layout(d)
+    if reset_before_dispatch:
+        step.reset()
+    step.dispatch(d)
+    step.experts()
+    step.combine(d)
+    return step, step.error(), guards
+
+
+def test_duplicate_expert_is_rejected_without_stray_writes():
+    w = wl.custom("dup", num_ranks=2, tokens_per_rank=8, hidden=128, num_experts=8, topk=2, max_m=8)
+    idx = wl.make_inputs(w).topk_idx.copy()
+    idx[1, 3, 1] = idx[1, 3, 0]
+    step, err, guards = _guarded_run(w, idx)
+    assert err == B.MOE_EINVAL
+    assert all(g.guards_intact() for g in guards)
+
+
+@pytest.mark.parametrize("bad", [8, -1, 1 << 30])
+def test_out_of_range_expert_is_rejected(bad):
+    w = wl.custom("oor", num_ranks=2, tokens_per_rank=8, hidden=128, num_experts=8, topk=2, max_m=8)
+    idx = wl.make_inputs(w).topk_idx.copy()
+    idx[0, 5, 0] = bad
+    step, err, guards = _guarded_run(w, idx)
+    assert err == B.MOE_EINVAL
+    assert int(step.buf.tok_slot[0, 5, 0]) == -1
+    assert all(g.guards_intact() for g in guards)
+
+
+def test_dispatch_without_layout_times_out():
+    """Zeroed count+1 flags: the bounded wait gives up, latches a timeout and writes nothing."""
+    w = wl.custom("noflags", num_ranks=2, tokens_per_rank=8, hidden=128, num_experts=8, topk=2, max_m=8)
+    idx = wl.make_inputs(w).topk_idx
+    step, err, guards = _guarded_run(w, idx, reset_before_dispatch=True)
+    assert err == B.MOE_ETIMEOUT
+    assert bool((step.buf.recv_meta == -7).all()), "no slot may be written without its count"
+    assert all(g.guards_intact() for g in guards)
+    # the context is still usable: a normal step succeeds afterwards
+    inp = wl.make_inputs(w)
+    step.reset()
+    step.run(P.to_device(inp, "cuda:0"))
+    assert step.error() == B.MOE_OK
+
+
+def test_host_validation():
+    w = wl.WORKLOADS["tiny"]
+    step = P.MoeStep(w, "cuda:0")
+    d = P.to_device(wl.make_inputs(w), "cuda:0")
+    bad = B.MoeDesc.of(w)
+    bad.tokens_per_rank = bad.max_m + 1
+    with pytest.raises(B.MoeError) as e:
+        B.moe_layout(bad, d.topk_idx, step.buf.counts, step.buf.flags, step.buf.tok_slot, step.buf.err)
+    assert e.value.status == B.MOE_EINVAL
+    # rows must start on a 16-byte boundary
+    xs = torch.empty(d.x.numel() * 2 + 8, dtype=torch.uint8, device="cuda:0")[2:2 + d.x.numel() * 2]
+    with pytest.raises(B.MoeError):
+        B.moe_dispatch(B.MoeDesc.of(w), xs, None, step.buf.tok_slot, step.buf.flags, step.buf.recv_x, None,
+                       step.buf.recv_meta, step.buf.err)
