@@ -12,8 +12,9 @@
 //
 // Design: one CTA of 128 threads per token; thread v handles 16-byte column
 // vectors v, v+128, ... of the row (8 bf16). For each vector it issues all k
-// streaming loads first (k x 16 B in flight per thread), then accumulates
-// w_j * y_j in fp32 with FMA in choice order j = 0..k-1 and stores the bf16
+// streaming loads first (k x 16 B in flight per thread), then forms
+// w_0 * y_0 and adds w_j * y_j in fp32 with FMA in choice order j = 1..k-1
+// (the sum starts from its first term, so signed zeros survive), and stores the bf16
 // (round to nearest even) result with a streaming store. Pure HBM gather:
 // no tensor cores, no shared-memory staging. Block 0 also clears the count+1
 // flags: dispatch, their only reader, finished before this kernel in stream
@@ -43,6 +44,15 @@ __device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float w, const uint4
   for (int q = 0; q < 4; ++q) {
     acc[2 * q] = fmaf(w, __uint_as_float(u[q] << 16), acc[2 * q]);
     acc[2 * q + 1] = fmaf(w, __uint_as_float(u[q] & 0xffff0000u), acc[2 * q + 1]);
+  }
+}
+
+__device__ __forceinline__ void mul_bf16x8(float (&acc)[8], float w, const uint4 &v) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    acc[2 * q] = __fmul_rn(w, __uint_as_float(u[q] << 16));
+    acc[2 * q + 1] = __fmul_rn(w, __uint_as_float(u[q] & 0xffff0000u));
   }
 }
 
@@ -101,9 +111,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
 #pragma unroll
     for (int j = 0; j < KC; ++j)
       if (j < k) y[j] = s_slot[j] >= 0 ? __ldcs(src[j] + v) : make_uint4(0, 0, 0, 0);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // the sum of the k terms starts from the first term (an all -0 token stays -0)
+    float acc[8];
+    mul_bf16x8(acc, w[0], y[0]);
 #pragma unroll
-    for (int j = 0; j < KC; ++j)
+    for (int j = 1; j < KC; ++j)
       if (j < k) fma_bf16x8(acc, w[j], y[j]);
     __stcs(dst + v, pack_bf16x8(acc));
   }

@@ -278,7 +278,9 @@ static int orc_cmp_slot(const void *a, const void *b) {
  * expert. [PPLX] combine: the receiver finds, through the routing table, which
  * slot to read for each expert and which weight to apply, and writes the
  * weighted sum into a caller-allocated tensor. The weights are applied at the
- * receiver, in fp64, and the sum is rounded to bf16 once.
+ * receiver, in fp64, and the sum is rounded to bf16 once. The sum starts from
+ * its first term (not from a +0 accumulator), so a token whose terms are all
+ * -0 keeps the sign of its zeros, as a sum of those terms does.
  *   y: n_slots rows of H bf16, row i being the expert output of slot slot_id[i];
  *   out: n_sel rows of H bf16 for the selected tokens sel[]. */
 int orc_combine(int R, int T, int H, int E, int k, int max_m, int64_t n_sel,
@@ -306,7 +308,6 @@ int orc_combine(int R, int T, int H, int E, int k, int max_m, int64_t n_sel,
       st = ORC_EINVAL;
       break;
     }
-    for (int h = 0; h < H; ++h) acc[h] = 0.0;
     for (int j = 0; j < k; ++j) {
       orc_slot_ref key = {tok_slot[tok * k + j], 0};
       const orc_slot_ref *hit = (const orc_slot_ref *)bsearch(
@@ -317,7 +318,10 @@ int orc_combine(int R, int T, int H, int E, int k, int max_m, int64_t n_sel,
       }
       double w = (double)weights[tok * k + j];
       const uint16_t *yr = y + hit->index * (int64_t)H;
-      for (int h = 0; h < H; ++h) acc[h] += w * orc_bf16_value(yr[h]);
+      for (int h = 0; h < H; ++h) {
+        double term = w * orc_bf16_value(yr[h]);
+        acc[h] = (j == 0) ? term : acc[h] + term; /* a sum of the k terms, no extra +0 */
+      }
     }
     for (int h = 0; h < H; ++h) out[i * (int64_t)H + h] = orc_bf16_from_double(acc[h]);
   }

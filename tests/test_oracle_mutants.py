@@ -22,7 +22,8 @@ MUTANTS = [
     ("expert factor wrong", "double c = 1.0 + (double)e / 256.0;", "double c = 1.0 + (double)e / 128.0;"),
     ("weight of the wrong choice", "double w = (double)weights[tok * k + j];",
      "double w = (double)weights[tok * k + (k - 1 - j)];"),
-    ("one expert dropped", "acc[h] += w * orc_bf16_value(yr[h]);", "acc[h] += (j ? w : 0.0) * orc_bf16_value(yr[h]);"),
+    ("one expert dropped", "acc[h] = (j == 0) ? term : acc[h] + term;", "acc[h] = (j == 0) ? 0.0 : acc[h] + term;"),
+    ("sum starts from +0", "acc[h] = (j == 0) ? term : acc[h] + term;", "acc[h] = (j == 0) ? 0.0 + term : acc[h] + term;"),
     ("truncation instead of rounding", "double r = rint(a / quantum) * quantum;",
      "double r = floor(a / quantum) * quantum;"),
     ("bf16 subnormal spacing", "if (e < -126) e = -126;", "if (e < -140) e = -140;"),

@@ -266,11 +266,13 @@ def _bf16_to_f64(bits):
 
 
 def test_combine_identity_experts_return_the_input(oracle_lib):
-    """Identity experts with weights that sum to 1 give back x exactly."""
+    """Identity experts with weights that sum to 1 give back x exactly, signed zeros included."""
     for w in (wl.WORKLOADS["tiny"],
               wl.custom("mix_small", num_ranks=4, tokens_per_rank=64, hidden=512, num_experts=8, topk=2,
                         max_m=64, x_dist="normal")):
         inp = wl.make_inputs(w)
+        inp.x.reshape(-1)[[3, 77, 500]] = 0x8000  # -0.0
+        inp.x.reshape(-1)[[5, 90]] = 0x0000       # +0.0
         res = oracle.run(w, inp)
         assert np.array_equal(res.out, inp.x.reshape(w.num_tokens, w.hidden))
 
