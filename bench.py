@@ -1,13 +1,14 @@
 #!/usr/bin/env python
 """Benchmark of MoE expert-parallel dispatch + combine on GB300.
 
-One step = layout -> dispatch -> combine over one batch of the DeepSeek-shape
-decode workload (8 logical EP ranks x 128 tokens, hidden 7168 fp8 e4m3 with
-128-element fp32 scales, 256 experts, top-8, max_m 128), inputs resident in
-HBM. The synthetic experts run once before timing (their outputs stay
-resident; layout is deterministic, so every step gathers valid rows). L2 is
-flushed (a memset of twice its size) before every timed step, outside the
-timed events.
+One step = layout + dispatch (one fused call) -> combine over one batch of the
+DeepSeek-shape decode workload (8 logical EP ranks x 128 tokens, hidden 7168
+fp8 e4m3 with 128-element fp32 scales, 256 experts, top-8, max_m 128), inputs
+resident in HBM (--unfused: layout and dispatch as two calls). The synthetic
+experts run once before timing (their outputs stay resident; layout is
+deterministic, so every step gathers valid rows). Before every timed step,
+outside the timed events, L2 is flushed: a buffer of twice its size is written
+and another one read, so each step starts from a cold L2 with no dirty lines.
 
 Arms:
   --impl native (default): the CUDA library through its C ABI; prints one JSON
@@ -202,17 +203,31 @@ def run_native(args, rank, local_rank, world):
         raise RuntimeError(f"first step failed: {B.moe_status_string(status)}")
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush_n = max(2 * l2, 256 << 20)
+    flush_w = torch.empty(flush_n, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(flush_n // 4, dtype=torch.int32, device=dev)
 
-    def path():
-        step.layout(d)
-        step.dispatch(d)
-        step.combine(d)
+    def flush():
+        # write a buffer twice the L2 size, then read another one: the timed step
+        # starts from a cold L2 that holds no dirty lines of the flush
+        flush_w.fill_(1)
+        flush_r.sum()
+
+    fused = not args.unfused
+    kernels = B.moe_layout_dispatch_kernels(step.desc) + 1 if fused else 3
+
+    def path(dd):
+        if fused:
+            step.layout_dispatch(dd)
+        else:
+            step.layout(dd)
+            step.dispatch(dd)
+        step.combine(dd)
 
     K, W = args.steps, args.warmup
     for _ in range(W):
-        flush.zero_()
-        path()
+        flush()
+        path(d)
     torch.cuda.synchronize()
     barrier(world)
 
@@ -221,58 +236,69 @@ def run_native(args, rank, local_rank, world):
     torch.cuda.synchronize()
     barrier(world)
     for i in range(K):
-        flush.zero_()
+        flush()
         ev[i][0].record(stream)
-        path()
+        path(d)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     step_ms = [a.elapsed_time(b) for a, b in ev]
 
     # per-kernel durations, CUDA events on the launching stream (a second pass of K steps)
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    stages = [("layout_dispatch", step.layout_dispatch)] if fused else \
+        [("layout", step.layout), ("dispatch", step.dispatch)]
+    stages.append(("combine", step.combine))
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
     for i in range(K):
-        flush.zero_()
+        flush()
         kev[i][0].record(stream)
-        step.layout(d)
-        kev[i][1].record(stream)
-        step.dispatch(d)
-        kev[i][2].record(stream)
-        step.combine(d)
-        kev[i][3].record(stream)
+        for j, (_, fn) in enumerate(stages):
+            fn(d)
+            kev[i][j + 1].record(stream)
     torch.cuda.synchronize()
-    kern_ms = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in kev)
-               for j, name in enumerate(("layout", "dispatch", "combine"))}
+    kern_ms = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in kev) for j, (name, _) in enumerate(stages)}
 
-    # end to end: host inputs in pinned memory, copies inside the timed region
+    # end to end: the step's inputs packed in one pinned host buffer, copied in
+    # with one H2D copy, and the output read back, all inside the timed region
     e2e = None
     if not args.no_e2e:
-        hx = torch.from_numpy(np.ascontiguousarray(inp.x)).pin_memory()
-        hidx = torch.from_numpy(inp.topk_idx).pin_memory()
-        hw = torch.from_numpy(inp.topk_weights).pin_memory()
-        hsc = torch.from_numpy(inp.x_scales).pin_memory() if inp.x_scales is not None else None
+        parts = [np.ascontiguousarray(inp.x).view(np.uint8).ravel(), inp.topk_idx.view(np.uint8).ravel(),
+                 inp.topk_weights.view(np.uint8).ravel()]
+        if inp.x_scales is not None:
+            parts.append(inp.x_scales.view(np.uint8).ravel())
+        offs, o = [], 0
+        for a_ in parts:
+            offs.append(o)
+            o += (a_.size + 255) // 256 * 256
+        hpack = torch.empty(o, dtype=torch.uint8).pin_memory()
+        for a_, off in zip(parts, offs):
+            hpack[off:off + a_.size].copy_(torch.from_numpy(a_))
+        dpack = torch.empty(o, dtype=torch.uint8, device=dev)
+
+        def view(i_, dtype, shape):
+            n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+            return dpack[offs[i_]:offs[i_] + n].view(dtype).view(shape)
+
+        R_, T_, H_, k_ = w.num_ranks, w.tokens_per_rank, w.hidden, w.topk
+        dx = view(0, torch.uint8 if w.dtype == "fp8" else torch.bfloat16, (R_, T_, H_))
+        d2 = P.DeviceInputs(view(1, torch.int32, (R_, T_, k_)), view(2, torch.float32, (R_, T_, k_)), dx,
+                            view(3, torch.float32, (R_, T_, H_ // 128)) if inp.x_scales is not None else None)
         hout = torch.empty((w.num_tokens, w.hidden), dtype=torch.bfloat16).pin_memory()
-        dx = d.x.view(torch.uint8) if d.x.dtype == torch.uint8 else d.x.view(torch.int16)
+        out_view = step.buf.out.view(w.num_tokens, w.hidden)
         eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         for i in range(K):
-            flush.zero_()
+            flush()
             eev[i][0].record(stream)
-            dx.copy_(hx.view(dx.dtype).view(dx.shape), non_blocking=True)
-            d.topk_idx.copy_(hidx, non_blocking=True)
-            d.topk_weights.copy_(hw, non_blocking=True)
-            if hsc is not None:
-                d.x_scales.copy_(hsc, non_blocking=True)
-            path()
-            hout.copy_(step.buf.out.view(w.num_tokens, w.hidden), non_blocking=True)
+            dpack.copy_(hpack, non_blocking=True)
+            path(d2)
+            hout.copy_(out_view, non_blocking=True)
             eev[i][1].record(stream)
         torch.cuda.synchronize()
         e2e_ms = sum(a.elapsed_time(b) for a, b in eev)
-        h2d = hx.numel() * hx.element_size() + hidx.numel() * 4 + hw.numel() * 4 + \
-            (hsc.numel() * 4 if hsc is not None else 0)
-        d2h = hout.numel() * 2
-        e2e = {"value": None, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "local_ms_total": e2e_ms}
-        if not torch.equal(hout.view(torch.int16), step.buf.out.view(w.num_tokens, w.hidden).cpu().view(torch.int16)):
+        e2e = {"value": None, "unit": "tokens/s", "h2d_bytes_per_step": int(sum(a_.size for a_ in parts)),
+               "d2h_bytes_per_step": hout.numel() * 2, "local_ms_total": e2e_ms,
+               "copies": "one pinned H2D copy of the packed inputs, one D2H copy of the bf16 output"}
+        if not torch.equal(hout.view(torch.int16), out_view.cpu().view(torch.int16)):
             raise RuntimeError("end-to-end output differs from the device output")
 
     clocks = sampler.stop()
@@ -290,16 +316,17 @@ def run_native(args, rank, local_rank, world):
     if rank != 0:
         return None
 
-    ab = w.algorithmic_bytes()
+    ab = dict(w.algorithmic_bytes())
+    ab["layout_dispatch"] = ab["layout"] + ab["dispatch"]
     peak, peak_kind = measured_hbm_peak()
     comb_s = kern_ms["combine"] / 1e3
     achieved = ab["combine"] / comb_s / 1e9
     traffic = profiled_traffic("moe_combine.cu", w.name)
-    kernels = {}
-    for name in ("layout", "dispatch", "combine"):
+    kernel_stats = {}
+    for name in kern_ms:
         gbs = ab[name] / (kern_ms[name] / 1e3) / 1e9
-        kernels[name] = {"us": round(kern_ms[name] * 1e3, 3), "algorithmic_bytes": ab[name], "GBps": round(gbs, 1),
-                         "frac_of_measured_hbm": round(gbs / peak, 4)}
+        kernel_stats[name] = {"us": round(kern_ms[name] * 1e3, 3), "algorithmic_bytes": ab[name],
+                              "GBps": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4)}
     step_s = job["ms_per_step"] / 1e3
     line = {
         "metric": METRIC,
@@ -322,7 +349,9 @@ def run_native(args, rank, local_rank, world):
             "algorithmic_bytes_per_step": ab["total"],
             "path": "layout (int32) -> dispatch (e4m3 rows + fp32 scales, byte copy) -> combine (bf16 in, fp32 "
                     "accumulate, bf16 out); synthetic experts outside the timed region",
-            "l2": "flushed before every timed step (memset of 2x L2, outside the timed events)",
+            "l2": "flushed before every timed step, outside the timed events: a write of a buffer of 2x L2 "
+                  "then a read of another (cold, clean L2)",
+            "step_kernels": "fused layout+dispatch, combine" if fused else "layout, dispatch, combine",
             "parallelism": "replicas only: one independent EP group of 8 logical ranks per GPU",
             "num_sms": args.num_sms,
         },
@@ -333,9 +362,10 @@ def run_native(args, rank, local_rank, world):
                      "peak": peak, "peak_kind": f"{peak_kind} (copy bandwidth)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": ab["combine"]},
-        "kernels": kernels,
+        "kernels": kernel_stats,
+        "kernel_timing": "CUDA events between the launches, a second pass of the same K steps",
         "e2e": e2e,
-        "gpu_launches": 3 * K,
+        "gpu_launches": kernels * K,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world >= 1:
@@ -434,6 +464,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("native", "reference"), default="native")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--num-sms", type=int, default=0)
+    ap.add_argument("--unfused", action="store_true", help="time layout and dispatch as two calls")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -26,6 +26,8 @@ from ._binding import (  # noqa: F401
     moe_expert_stub,
     moe_get_error,
     moe_layout,
+    moe_layout_dispatch,
+    moe_layout_dispatch_kernels,
     moe_reset,
     moe_status_string,
 )

@@ -66,14 +66,17 @@ def load():
     lib.moe_buffer_sizes.argtypes = [pdesc, ctypes.POINTER(MoeSizes)]
     lib.moe_layout.argtypes = [pdesc] + [vp] * 6
     lib.moe_dispatch.argtypes = [pdesc] + [vp] * 9
+    lib.moe_layout_dispatch.argtypes = [pdesc] + [vp] * 11
     lib.moe_expert_stub.argtypes = [pdesc] + [vp] * 6
     lib.moe_combine.argtypes = [pdesc] + [vp] * 7
     lib.moe_reset.argtypes = [pdesc] + [vp] * 3
     lib.moe_get_error.argtypes = [vp, vp]
+    lib.moe_layout_dispatch_kernels.argtypes = [pdesc]
+    lib.moe_layout_dispatch_kernels.restype = ctypes.c_int32
     lib.moe_status_string.argtypes = [ctypes.c_int32]
     lib.moe_status_string.restype = ctypes.c_char_p
-    for name in ("moe_buffer_sizes", "moe_layout", "moe_dispatch", "moe_expert_stub", "moe_combine", "moe_reset",
-                 "moe_get_error"):
+    for name in ("moe_buffer_sizes", "moe_layout", "moe_dispatch", "moe_layout_dispatch", "moe_expert_stub",
+                 "moe_combine", "moe_reset", "moe_get_error"):
         getattr(lib, name).restype = st
     _lib = lib
     return lib
@@ -118,6 +121,19 @@ def moe_dispatch(desc, x, x_scales, tok_slot, flags, recv_x, recv_scales, recv_m
     _check(load().moe_dispatch(ctypes.byref(desc), _ptr(x), _ptr(x_scales), _ptr(tok_slot), _ptr(flags),
                                _ptr(recv_x), _ptr(recv_scales), _ptr(recv_meta), _ptr(err), _stream(stream)),
            "moe_dispatch")
+
+
+def moe_layout_dispatch(desc, topk_idx, x, x_scales, counts, flags, tok_slot, recv_x, recv_scales, recv_meta, err,
+                        stream=None):
+    _check(load().moe_layout_dispatch(ctypes.byref(desc), _ptr(topk_idx), _ptr(x), _ptr(x_scales), _ptr(counts),
+                                      _ptr(flags), _ptr(tok_slot), _ptr(recv_x), _ptr(recv_scales), _ptr(recv_meta),
+                                      _ptr(err), _stream(stream)), "moe_layout_dispatch")
+
+
+def moe_layout_dispatch_kernels(desc) -> int:
+    n = int(load().moe_layout_dispatch_kernels(ctypes.byref(desc)))
+    _check(min(n, 0), "moe_layout_dispatch_kernels")
+    return n
 
 
 def moe_expert_stub(desc, recv_x, recv_scales, counts, expert_out, err, stream=None):

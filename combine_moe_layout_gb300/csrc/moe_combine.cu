@@ -10,15 +10,17 @@
 // combine is also the step's only barrier. "NVSHMEM and DeepEP", high-throughput
 // section: combine returns BF16.
 //
-// Design: one CTA of 128 threads per token; thread v handles 16-byte column
-// vectors v, v+128, ... of the row (8 bf16). For each vector it issues all k
-// streaming loads first (k x 16 B in flight per thread), then forms
-// w_0 * y_0 and adds w_j * y_j in fp32 with FMA in choice order j = 1..k-1
-// (the sum starts from its first term, so signed zeros survive), and stores the bf16
-// (round to nearest even) result with a streaming store. Pure HBM gather:
-// no tensor cores, no shared-memory staging. Block 0 also clears the count+1
-// flags: dispatch, their only reader, finished before this kernel in stream
-// order, so the next layout signals afresh.
+// Design: the work is (token, 16-byte column vector) tasks, 8 bf16 each. A
+// block of 128 threads covers 128*VPT consecutive vectors of one token; each
+// thread loads the token's k slot ids and weights (warp-broadcast loads), issues
+// all k x VPT streaming 16-byte loads of its vectors first, then forms w_0*y_0
+// and adds w_j*y_j in fp32 with FMA in choice order j = 1..k-1 (the sum starts
+// from its first term, so signed zeros survive) and stores bf16 (round to
+// nearest even) with a streaming store. The grid is all tasks, so waves of
+// blocks overlap and keep enough bytes in flight to cover HBM latency. Pure
+// HBM gather: no tensor cores, no shared memory. Block 0 also clears the
+// count+1 flags: dispatch, their only reader, finished before this kernel in
+// stream order, so the next layout signals afresh.
 #include <cuda_bf16.h>
 
 #include "moe_common.cuh"
@@ -34,7 +36,7 @@ struct CombineArgs {
   uint64_t *flags;
   uint16_t *out;
   int32_t *err;
-  int H, k, nflags;
+  int H, k, nflags, chunks;
   int64_t nslots;
 };
 
@@ -67,65 +69,73 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
 }
 
 // K > 0: compile-time number of choices; K == 0: runtime k (<= kMaxTopk).
-template <int K>
+// Block b handles token b / chunks, column vectors [c*128*VPT, (c+1)*128*VPT)
+// with c = b % chunks; each thread owns VPT vectors and issues all their k
+// loads before it computes.
+template <int K, int VPT>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a) {
   constexpr int KC = K > 0 ? K : kMaxTopk;
-  __shared__ int32_t s_slot[KC];
-  __shared__ float s_w[KC];
   const int k = K > 0 ? K : a.k;
-  const int64_t tok = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int64_t b = blockIdx.x;
+  const int64_t tok = b / a.chunks;
+  const int v0 = static_cast<int>(b % a.chunks) * kCombineThreads * VPT + threadIdx.x;
+  const int V = a.H / 8;
 
   grid_dependency_wait();
-  if (blockIdx.x == 0)
-    for (int i = tid; i < a.nflags; i += blockDim.x) a.flags[i] = 0;
+  grid_dependents_launch();
+  if (b == 0)
+    for (int i = threadIdx.x; i < a.nflags; i += blockDim.x) a.flags[i] = 0;
 
-  if (tid < k) {
-    int32_t slot = __ldg(a.tok_slot + tok * k + tid);
-    float w = __ldg(a.weights + tok * k + tid);
-    if (slot >= a.nslots) {
-      latch_error(a.err, MOE_EINVAL);
-      slot = -1;
-    }
-    if (slot < 0) w = 0.0f;  // an entry layout rejected contributes nothing
-    s_slot[tid] = slot;
-    s_w[tid] = w;
-  }
-  __syncthreads();
-
-  const int V = a.H / 8;
-  const uint4 *src[KC];
+  // this token's slots and weights (the same for the whole warp: broadcast loads)
+  int32_t slot[KC];
   float w[KC];
 #pragma unroll
   for (int j = 0; j < KC; ++j) {
     if (j < k) {
-      const int32_t slot = s_slot[j];
-      src[j] = reinterpret_cast<const uint4 *>(a.y + static_cast<int64_t>(slot < 0 ? 0 : slot) * a.H);
-      w[j] = s_w[j];
+      slot[j] = __ldg(a.tok_slot + tok * k + j);
+      w[j] = __ldg(a.weights + tok * k + j);
+      if (slot[j] >= a.nslots) {
+        latch_error(a.err, MOE_EINVAL);
+        slot[j] = -1;
+      }
+      if (slot[j] < 0) w[j] = 0.0f;  // an entry layout rejected contributes nothing
     }
   }
-  uint4 *dst = reinterpret_cast<uint4 *>(a.out + tok * a.H);
 
-  for (int v = tid; v < V; v += kCombineThreads) {
-    uint4 y[KC];
+  uint4 y[VPT][KC];
+#pragma unroll
+  for (int u = 0; u < VPT; ++u) {
+    const int v = v0 + u * kCombineThreads;
 #pragma unroll
     for (int j = 0; j < KC; ++j)
-      if (j < k) y[j] = s_slot[j] >= 0 ? __ldcs(src[j] + v) : make_uint4(0, 0, 0, 0);
+      if (j < k)
+        y[u][j] = (v < V && slot[j] >= 0)
+                      ? __ldcs(reinterpret_cast<const uint4 *>(a.y + static_cast<int64_t>(slot[j]) * a.H) + v)
+                      : make_uint4(0, 0, 0, 0);
+  }
+  uint4 *dst = reinterpret_cast<uint4 *>(a.out + tok * a.H);
+#pragma unroll
+  for (int u = 0; u < VPT; ++u) {
+    const int v = v0 + u * kCombineThreads;
+    if (v >= V) break;
     // the sum of the k terms starts from the first term (an all -0 token stays -0)
     float acc[8];
-    mul_bf16x8(acc, w[0], y[0]);
+    mul_bf16x8(acc, w[0], y[u][0]);
 #pragma unroll
     for (int j = 1; j < KC; ++j)
-      if (j < k) fma_bf16x8(acc, w[j], y[j]);
+      if (j < k) fma_bf16x8(acc, w[j], y[u][j]);
     __stcs(dst + v, pack_bf16x8(acc));
   }
-  grid_dependents_launch();
 }
 
-template <int K>
-moe_status launch_combine_k(const CombineArgs &a, int64_t ntok, cudaStream_t stream) {
+template <int K, int VPT>
+moe_status launch_combine_k(CombineArgs a, int64_t ntok, cudaStream_t stream) {
+  const int V = a.H / 8;
+  a.chunks = (V + kCombineThreads * VPT - 1) / (kCombineThreads * VPT);
+  const int64_t blocks = ntok * a.chunks;
+  if (blocks > 0x7fffffffll) return MOE_EINVAL;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(ntok), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
   cfg.blockDim = dim3(kCombineThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -134,13 +144,13 @@ moe_status launch_combine_k(const CombineArgs &a, int64_t ntok, cudaStream_t str
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, combine_kernel<K>, a) != cudaSuccess) return MOE_ECUDA;
+  if (cudaLaunchKernelEx(&cfg, combine_kernel<K, VPT>, a) != cudaSuccess) return MOE_ECUDA;
   return launch_status();
 }
 
 moe_status launch_combine(const Sizes &s, const uint16_t *y, const float *weights, const int32_t *tok_slot,
                           uint64_t *flags, uint16_t *out, int32_t *err, cudaStream_t stream) {
-  CombineArgs a{y, weights, tok_slot, flags, out, err, s.H, s.k, s.E * s.R, s.nslots};
+  CombineArgs a{y, weights, tok_slot, flags, out, err, s.H, s.k, s.E * s.R, 1, s.nslots};
   if (s.ntok == 0) {
     // nothing to gather; still clear the flags for the next step
     if (cudaMemsetAsync(flags, 0, static_cast<size_t>(s.E) * s.R * sizeof(uint64_t), stream) != cudaSuccess)
@@ -148,12 +158,12 @@ moe_status launch_combine(const Sizes &s, const uint16_t *y, const float *weight
     return MOE_OK;
   }
   switch (s.k) {
-    case 1: return launch_combine_k<1>(a, s.ntok, stream);
-    case 2: return launch_combine_k<2>(a, s.ntok, stream);
-    case 4: return launch_combine_k<4>(a, s.ntok, stream);
-    case 6: return launch_combine_k<6>(a, s.ntok, stream);
-    case 8: return launch_combine_k<8>(a, s.ntok, stream);
-    default: return launch_combine_k<0>(a, s.ntok, stream);
+    case 1: return launch_combine_k<1, 2>(a, s.ntok, stream);
+    case 2: return launch_combine_k<2, 2>(a, s.ntok, stream);
+    case 4: return launch_combine_k<4, 1>(a, s.ntok, stream);
+    case 6: return launch_combine_k<6, 1>(a, s.ntok, stream);
+    case 8: return launch_combine_k<8, 1>(a, s.ntok, stream);
+    default: return launch_combine_k<0, 1>(a, s.ntok, stream);
   }
 }
 

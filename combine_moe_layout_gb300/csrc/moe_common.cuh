@@ -9,6 +9,7 @@
 namespace moe {
 
 constexpr int kMaxTopk = 16;
+constexpr int kMaxStages = 8;  // row stages of the dispatch kernels
 constexpr int kScaleBlock = 128;  // elements per fp32 scale of an fp8 row
 
 // Limits of the bounded waits, in nanoseconds of %globaltimer. A count+1 flag
@@ -186,5 +187,19 @@ inline moe_status launch_status() { return cudaGetLastError() == cudaSuccess ? M
 
 // SM count of the current device (queried once per device).
 int sm_count();
+
+// Units issued but not yet consumed when a pipelined loop aborts at unit i:
+// the prologue issued units [0, S), and iteration u >= 1 refilled unit u-1+S,
+// so the loads of units [i, end) may still be in flight.
+__host__ __device__ inline int64_t inflight_end(int64_t i, int64_t S, int64_t n) {
+  const int64_t end = i == 0 ? S : i - 1 + S;
+  return end < n ? end : n;
+}
+
+moe_status launch_layout(const Sizes &s, const int32_t *topk_idx, int32_t *counts, uint64_t *flags,
+                         int32_t *tok_slot, int32_t *err, cudaStream_t stream);
+moe_status launch_dispatch(const Sizes &s, const void *x, const float *x_scales, const int32_t *tok_slot,
+                           const uint64_t *flags, void *recv_x, float *recv_scales, int32_t *recv_meta,
+                           int32_t *err, int num_sms, cudaStream_t stream);
 
 }  // namespace moe

@@ -25,7 +25,6 @@ namespace moe {
 
 constexpr uint32_t kPieceMax = 16384;       // bytes staged per unit
 constexpr uint32_t kStageBudget = 32768;    // shared bytes of staging per CTA
-constexpr int kMaxStages = 8;
 
 struct DispatchArgs {
   const uint8_t *x;
@@ -66,11 +65,14 @@ __global__ void __launch_bounds__(32) dispatch_kernel(DispatchArgs a) {
     aborted = 0;
   }
   __syncwarp();
-  grid_dependency_wait();
-
+  // The rows are inputs that layout does not write: start loading them while
+  // the layout kernel may still run (programmatic dependent launch), then wait
+  // for its slot ids and flags.
   if (lane == 0)
     for (int64_t i = 0; i < n_mine && i < S; ++i)
       issue_unit_load(a, dsm + static_cast<size_t>(i) * a.piece_bytes, &full[i], first + i * stride);
+  grid_dependency_wait();
+  grid_dependents_launch();
 
   int64_t i = 0;
   for (; i < n_mine; ++i) {
@@ -140,17 +142,14 @@ __global__ void __launch_bounds__(32) dispatch_kernel(DispatchArgs a) {
 
   if (lane == 0) {
     if (aborted) {
-      // Drain the loads still in flight (bounded) before the CTA releases its
-      // shared memory: units i .. i+S-2 were issued (the refill of unit i-1+S
-      // had not happened yet).
-      const int64_t issued = n_mine < i + S - 1 ? n_mine : i + S - 1;
+      // drain the loads still in flight (bounded) before the CTA releases its shared memory
+      const int64_t issued = inflight_end(i, S, n_mine);
       for (int64_t u = i; u < issued; ++u)
         mbar_wait_bounded(&full[u % S], static_cast<uint32_t>((u / S) & 1));
     }
     bulk_wait_all();
   }
   __syncwarp();
-  grid_dependents_launch();
 }
 
 moe_status launch_dispatch(const Sizes &s, const void *x, const float *x_scales, const int32_t *tok_slot,

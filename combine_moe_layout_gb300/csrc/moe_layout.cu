@@ -17,8 +17,11 @@
 //   2. it builds a 128-bit membership bitmap per expert for its own chunk
 //      (a repeated expert in one token shows up as a bit already set);
 //   3. pos = base + popcount of the bitmap below the token;
-//   4. the last chunk of a source rank owns the totals and publishes counts and
-//      flags = count + 1 with release stores.
+//   4. the last chunk of a source rank owns the totals and writes counts and
+//      flags = count + 1. Consumers are later kernels in stream order, which
+//      see them once this grid completes (griddepcontrol.wait under
+//      programmatic dependent launch), so plain stores suffice: a release fence
+//      per flag would only lengthen this latency-bound kernel.
 #include <cstdio>
 
 #include "moe_common.cuh"
@@ -50,6 +53,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
 
   grid_dependency_wait();
+  grid_dependents_launch();  // dispatch may start loading its rows meanwhile
   for (int i = tid; i < a.E * (1 + kLayoutWords); i += blockDim.x) lsm[i] = 0;
   __syncthreads();
 
@@ -111,10 +115,9 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
       for (int w = 0; w < kLayoutWords; ++w) c += __popc(bits[e * kLayoutWords + w]);
       const int64_t r = static_cast<int64_t>(e) * a.R + src;
       a.counts[r] = c;
-      store_release_u64(a.flags + r, static_cast<uint64_t>(c) + 1);
+      a.flags[r] = static_cast<uint64_t>(c) + 1;
     }
   }
-  grid_dependents_launch();
 }
 
 int sm_count() {

@@ -65,6 +65,11 @@ class MoeStep:
         B.moe_dispatch(self.desc, d.x, d.x_scales, b.tok_slot, b.flags, b.recv_x, b.recv_scales, b.recv_meta, b.err,
                        stream)
 
+    def layout_dispatch(self, d: DeviceInputs, stream=None):
+        b = self.buf
+        B.moe_layout_dispatch(self.desc, d.topk_idx, d.x, d.x_scales, b.counts, b.flags, b.tok_slot, b.recv_x,
+                              b.recv_scales, b.recv_meta, b.err, stream)
+
     def experts(self, stream=None):
         if self.fp8:
             b = self.buf
@@ -74,9 +79,12 @@ class MoeStep:
         b = self.buf
         B.moe_combine(self.desc, self.y, d.topk_weights, b.tok_slot, b.flags, b.out, b.err, stream)
 
-    def run(self, d: DeviceInputs, stream=None):
-        self.layout(d, stream)
-        self.dispatch(d, stream)
+    def run(self, d: DeviceInputs, stream=None, fused: bool = False):
+        if fused:
+            self.layout_dispatch(d, stream)
+        else:
+            self.layout(d, stream)
+            self.dispatch(d, stream)
         self.experts(stream)
         self.combine(d, stream)
 

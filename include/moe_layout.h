@@ -37,6 +37,12 @@
  *     moe_get_error. Kernels never trap: they skip the offending access.
  *   - One step is moe_layout -> moe_dispatch -> (the caller's experts) ->
  *     moe_combine, in stream order on one stream.
+ *   - The kernels use programmatic dependent launch: each may be scheduled
+ *     while the kernel before it in the stream finishes, and waits for that
+ *     kernel's results before touching them. moe_dispatch starts reading x (an
+ *     input that moe_layout never writes) before that wait, so x must be
+ *     complete before moe_layout is enqueued (as it is when x comes from a copy
+ *     or a kernel enqueued earlier).
  */
 #ifndef MOE_LAYOUT_H
 #define MOE_LAYOUT_H
@@ -122,6 +128,22 @@ moe_status moe_layout(const moe_desc *desc, const int32_t *topk_idx, int32_t *co
 moe_status moe_dispatch(const moe_desc *desc, const void *x, const float *x_scales, const int32_t *tok_slot,
                         const uint64_t *flags, void *recv_x, float *recv_scales, int32_t *recv_meta,
                         int32_t *err, void *stream);
+
+/* Layout and dispatch in one call: the same outputs as moe_layout followed by
+ * moe_dispatch (same arguments, same device errors except that no flag wait
+ * can time out). When one CTA can hold a source rank's per-expert token
+ * bitmaps (T <= 1024, rows of at most 16 KiB) it runs as one kernel in which
+ * every CTA computes its rows' slots itself while their bulk loads are in
+ * flight (Perplexity, "Dispatch": the counting warp beside the packing warps);
+ * otherwise it launches the two kernels. */
+moe_status moe_layout_dispatch(const moe_desc *desc, const int32_t *topk_idx, const void *x, const float *x_scales,
+                               int32_t *counts, uint64_t *flags, int32_t *tok_slot, void *recv_x,
+                               float *recv_scales, int32_t *recv_meta, int32_t *err, void *stream);
+
+/* Number of kernels one moe_layout_dispatch call launches for this desc (1 or
+ * 2; an empty batch launches only the layout kernel), or MOE_EINVAL.
+ * Host-only. */
+int32_t moe_layout_dispatch_kernels(const moe_desc *desc);
 
 /* Synthetic experts for tests and benchmarks (not part of the pages' method):
  * for every filled slot (pos < counts) of an fp8 step,

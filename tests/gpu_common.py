@@ -67,8 +67,9 @@ def guarded_buffers(desc, device):
     return bufs, [v for v in g.values() if v is not None]
 
 
-def run_step(w, inp, device="cuda:0", num_sms=0, guards=False):
-    """layout -> dispatch -> experts -> combine; returns (step, flags after layout, error, guard list)."""
+def run_step(w, inp, device="cuda:0", num_sms=0, guards=False, fused=False):
+    """layout -> dispatch (or the fused call) -> experts -> combine; returns
+    (step, device inputs, flags after layout, error, guard list)."""
     desc = B.MoeDesc.of(w, num_sms)
     glist = []
     if guards:
@@ -82,9 +83,13 @@ def run_step(w, inp, device="cuda:0", num_sms=0, guards=False):
         step.buf.recv_x.fill_(POISON_BYTE)
     d = P.to_device(inp, device)
     step.reset()
-    step.layout(d)
-    flags = step.buf.flags.clone()
-    step.dispatch(d)
+    if fused:
+        step.layout_dispatch(d)
+        flags = step.buf.flags.clone()
+    else:
+        step.layout(d)
+        flags = step.buf.flags.clone()
+        step.dispatch(d)
     step.experts()
     step.combine(d)
     err = step.error()

@@ -22,7 +22,8 @@ def declared_functions():
 
 def test_header_declares_the_path():
     names = declared_functions()
-    for n in ("moe_buffer_sizes", "moe_layout", "moe_dispatch", "moe_combine", "moe_get_error", "moe_reset"):
+    for n in ("moe_buffer_sizes", "moe_layout", "moe_dispatch", "moe_layout_dispatch", "moe_combine",
+              "moe_get_error", "moe_reset"):
         assert n in names
 
 
@@ -72,3 +73,11 @@ def test_status_strings():
     for code in (0, -1, -2, -3, -4, -5):
         assert B.moe_status_string(code) != "unknown status"
     assert B.moe_status_string(99) == "unknown status"
+
+
+def test_fused_kernel_count_is_a_host_query():
+    decode = B.MoeDesc(8, 128, 7168, 256, 8, 128, 1, 0)
+    prefill = B.MoeDesc(8, 4096, 7168, 256, 8, 4096, 1, 0)
+    assert B.moe_layout_dispatch_kernels(decode) == 1
+    assert B.moe_layout_dispatch_kernels(prefill) == 2
+    assert B.moe_layout_dispatch_kernels(B.MoeDesc(8, 0, 7168, 256, 8, 128, 1, 0)) == 1

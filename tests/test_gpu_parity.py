@@ -37,9 +37,9 @@ def _sample(w, n, seed=7):
     return np.unique(np.concatenate([s, [0, N - 1]])).astype(np.int64)
 
 
-def _full_parity(w, inp, num_sms=0, region_sets=True):
+def _full_parity(w, inp, num_sms=0, region_sets=True, fused=False):
     ref = oracle.run(w, inp)
-    step, d, flags, err, _ = run_step(w, inp, num_sms=num_sms)
+    step, d, flags, err, _ = run_step(w, inp, num_sms=num_sms, fused=fused)
     assert err == B.MOE_OK, B.moe_status_string(err)
     ts = check_layout(step, flags, ref, w)
     check_dispatch(step, w, ts, ref)
@@ -53,29 +53,38 @@ def _full_parity(w, inp, num_sms=0, region_sets=True):
     return step, d, ref, out
 
 
-def test_tiny():
+FUSED = [False, True]
+FUSED_IDS = ["separate", "fused"]
+
+
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+def test_tiny(fused):
     w = wl.WORKLOADS["tiny"]
     inp = wl.make_inputs(w)
-    step, d, ref, out = _full_parity(w, inp)
+    step, d, ref, out = _full_parity(w, inp, fused=fused)
     # identity experts, renormalised weights: combine returns the input
     assert np.array_equal(out, inp.x.reshape(w.num_tokens, w.hidden))
 
 
-def test_ds_decode():
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+def test_ds_decode(fused):
     w = wl.WORKLOADS["ds_decode"]
-    _full_parity(w, wl.make_inputs(w), region_sets=False)
+    if fused:
+        assert B.moe_layout_dispatch_kernels(B.MoeDesc.of(w)) == 1
+    _full_parity(w, wl.make_inputs(w), region_sets=False, fused=fused)
 
 
-def test_skewed():
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+def test_skewed(fused):
     w = wl.WORKLOADS["skewed"]
     inp = wl.make_inputs(w)
-    step, d, ref, out = _full_parity(w, inp, region_sets=False)
+    step, d, ref, out = _full_parity(w, inp, region_sets=False, fused=fused)
     assert np.array_equal(out, inp.x.reshape(w.num_tokens, w.hidden))
     # the hot expert fills nearly all of rank 0's slots for it
     assert ref.counts[0].max() > 0.9 * w.tokens_per_rank
 
 
-def _large_parity(w, n_sample):
+def _large_parity(w, n_sample, fused=False):
     inp = wl.make_inputs(w)
     sel = _sample(w, n_sample)
     counts, flags, tok_slot = oracle.layout(inp.topk_idx, w.num_experts, w.max_m)
@@ -84,7 +93,7 @@ def _large_parity(w, n_sample):
     y = oracle.expert_stub(slots, w.num_ranks, w.hidden, w.num_experts, w.max_m, dt)
     out_ref = oracle.combine(tok_slot, inp.topk_weights, slots.slot_id, y, w.num_experts, w.max_m, sel)
     ref = oracle.OracleResult(counts, flags, tok_slot, slots, y, out_ref, sel)
-    step, d, fl, err, _ = run_step(w, inp)
+    step, d, fl, err, _ = run_step(w, inp, fused=fused)
     assert err == B.MOE_OK, B.moe_status_string(err)
     ts = check_layout(step, fl, ref, w)
     check_dispatch(step, w, ts, ref)
@@ -95,9 +104,12 @@ def _large_parity(w, n_sample):
     return step, d, inp
 
 
-def test_mixtral():
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+def test_mixtral(fused):
     w = wl.WORKLOADS["mixtral"]
-    step, d, inp = _large_parity(w, 2048)
+    if fused:  # 4096 tokens per rank: the fused call runs the two kernels
+        assert B.moe_layout_dispatch_kernels(B.MoeDesc.of(w)) == 2
+    step, d, inp = _large_parity(w, 2048, fused=fused)
     # every token: identity experts with renormalised weights give back x exactly
     assert torch.equal(step.buf.out.view(torch.int16), d.x.view(torch.int16))
 
@@ -154,18 +166,31 @@ EDGE = {
 }
 
 
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
 @pytest.mark.parametrize("name", list(EDGE))
-def test_edge_shapes(name):
+def test_edge_shapes(name, fused):
     w = wl.custom(name, **EDGE[name])
-    _full_parity(w, wl.make_inputs(w, seed=3), region_sets=w.num_experts * w.num_ranks * w.max_m * w.row_bytes < (1 << 28))
+    small = w.num_experts * w.num_ranks * w.max_m * w.row_bytes < (1 << 28)
+    _full_parity(w, wl.make_inputs(w, seed=3), region_sets=small, fused=fused)
 
 
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
 @pytest.mark.parametrize("num_sms", [1, 3])
-def test_few_sms_deep_pipeline(num_sms):
+def test_few_sms_deep_pipeline(num_sms, fused):
     """With one or three SMs every dispatch CTA streams many rows through its stages."""
     w = wl.custom("deep", num_ranks=4, tokens_per_rank=200, hidden=2048, num_experts=16, topk=4, max_m=200,
                   x_dist="normal")
-    _full_parity(w, wl.make_inputs(w, seed=5), num_sms=num_sms, region_sets=False)
+    if fused:
+        assert B.moe_layout_dispatch_kernels(B.MoeDesc.of(w, num_sms)) == 1
+    _full_parity(w, wl.make_inputs(w, seed=5), num_sms=num_sms, region_sets=False, fused=fused)
+
+
+def test_fused_max_tokens_per_rank():
+    """1024 tokens per rank: the largest batch the fused kernel takes, with several rows per CTA."""
+    w = wl.custom("fused_max", num_ranks=4, tokens_per_rank=1024, hidden=1024, num_experts=64, topk=8, max_m=1024,
+                  dtype="fp8", expert="scale", x_dist="normal", renormalize=False)
+    assert B.moe_layout_dispatch_kernels(B.MoeDesc.of(w)) == 1
+    _full_parity(w, wl.make_inputs(w, seed=9), region_sets=False, fused=True)
 
 
 def test_empty_batch():
@@ -178,7 +203,8 @@ def test_empty_batch():
     assert all(g.guards_intact() for g in guards)
 
 
-def test_repeated_steps_reuse_buffers():
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+def test_repeated_steps_reuse_buffers(fused):
     """Combine clears the flags, so the same buffers serve the next step."""
     w = wl.custom("rep", num_ranks=4, tokens_per_rank=50, hidden=512, num_experts=16, topk=4, max_m=64,
                   dtype="fp8", expert="scale", x_dist="normal")
@@ -188,7 +214,7 @@ def test_repeated_steps_reuse_buffers():
         inp = wl.make_inputs(w, seed=seed)
         ref = oracle.run(w, inp)
         d = P.to_device(inp, "cuda:0")
-        step.run(d)
+        step.run(d, fused=fused)
         assert step.error() == B.MOE_OK
         out = step.buf.out.view(torch.int16).cpu().numpy().view(np.uint16).reshape(w.num_tokens, w.hidden)
         assert_combine_close(out, ref.out)
@@ -211,7 +237,7 @@ def test_layout_is_deterministic():
 
 # --- error paths (no fault, no trap: the kernels latch a status and skip) ----------
 
-def _guarded_run(w, topk_idx, stages=("layout", "dispatch", "experts", "combine"), reset_before_dispatch=False):
+def _guarded_run(w, topk_idx, reset_before_dispatch=False, fused=False):
     inp = wl.make_inputs(w)
     inp.topk_idx[...] = topk_idx
     step, d, flags, err, guards = None, None, None, None, None
@@ -221,30 +247,35 @@ def _guarded_run(w, topk_idx, stages=("layout", "dispatch", "experts", "combine"
     step = P.MoeStep(w, "cuda:0", buffers=bufs)
     d = P.to_device(inp, "cuda:0")
     step.reset()
-    step.layout(d)
-    if reset_before_dispatch:
-        step.reset()
-    step.dispatch(d)
+    if fused:
+        step.layout_dispatch(d)
+    else:
+        step.layout(d)
+        if reset_before_dispatch:
+            step.reset()
+        step.dispatch(d)
     step.experts()
     step.combine(d)
     return step, step.error(), guards
 
 
-def test_duplicate_expert_is_rejected_without_stray_writes():
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+def test_duplicate_expert_is_rejected_without_stray_writes(fused):
     w = wl.custom("dup", num_ranks=2, tokens_per_rank=8, hidden=128, num_experts=8, topk=2, max_m=8)
     idx = wl.make_inputs(w).topk_idx.copy()
     idx[1, 3, 1] = idx[1, 3, 0]
-    step, err, guards = _guarded_run(w, idx)
+    step, err, guards = _guarded_run(w, idx, fused=fused)
     assert err == B.MOE_EINVAL
     assert all(g.guards_intact() for g in guards)
 
 
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
 @pytest.mark.parametrize("bad", [8, -1, 1 << 30])
-def test_out_of_range_expert_is_rejected(bad):
+def test_out_of_range_expert_is_rejected(bad, fused):
     w = wl.custom("oor", num_ranks=2, tokens_per_rank=8, hidden=128, num_experts=8, topk=2, max_m=8)
     idx = wl.make_inputs(w).topk_idx.copy()
     idx[0, 5, 0] = bad
-    step, err, guards = _guarded_run(w, idx)
+    step, err, guards = _guarded_run(w, idx, fused=fused)
     assert err == B.MOE_EINVAL
     assert int(step.buf.tok_slot[0, 5, 0]) == -1
     assert all(g.guards_intact() for g in guards)
