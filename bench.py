@@ -205,7 +205,7 @@ def run_native(args, rank, local_rank, world):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_n = max(2 * l2, 256 << 20)
     flush_w = torch.empty(flush_n, dtype=torch.uint8, device=dev)
-    flush_r = torch.ones(flush_n // 4, dtype=torch.int32, device=dev)
+    flush_r = torch.ones(flush_n // 4, dtype=torch.float32, device=dev)
 
     def flush():
         # write a buffer twice the L2 size, then read another one: the timed step
@@ -231,6 +231,19 @@ def run_native(args, rank, local_rank, world):
     torch.cuda.synchronize()
     barrier(world)
 
+    timed = lambda: path(d)  # noqa: E731
+    if args.graph:
+        # the step's launches captured once into a CUDA graph and replayed
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            path(d)
+        torch.cuda.synchronize()
+        timed = graph.replay
+        for _ in range(W):
+            flush()
+            timed()
+        torch.cuda.synchronize()
+
     sampler = ClockSampler(local_rank).start()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     torch.cuda.synchronize()
@@ -238,7 +251,7 @@ def run_native(args, rank, local_rank, world):
     for i in range(K):
         flush()
         ev[i][0].record(stream)
-        path(d)
+        timed()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -352,6 +365,7 @@ def run_native(args, rank, local_rank, world):
             "l2": "flushed before every timed step, outside the timed events: a write of a buffer of 2x L2 "
                   "then a read of another (cold, clean L2)",
             "step_kernels": "fused layout+dispatch, combine" if fused else "layout, dispatch, combine",
+            "launch": "one CUDA graph replay per step" if args.graph else "direct launches through the C ABI",
             "parallelism": "replicas only: one independent EP group of 8 logical ranks per GPU",
             "num_sms": args.num_sms,
         },
@@ -456,6 +470,44 @@ def run_reference(args, rank, local_rank, world):
     }
 
 
+def calibrate(local_rank: int) -> dict:
+    """Bandwidth of torch's fill (write only) and copy (read + write) kernels over
+    a range of sizes around the step's, timed like the step (L2 flushed before each)."""
+    import torch
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(flush_w.numel() // 4, dtype=torch.float32, device=dev)
+
+    def timeit(fn, n=100):
+        for _ in range(5):
+            flush_w.fill_(1)
+            flush_r.sum()
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in ev:
+            flush_w.fill_(1)
+            flush_r.sum()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
+
+    rows = []
+    for mb in (15, 30, 60, 120, 240, 480, 960):
+        a = torch.empty(mb << 20, dtype=torch.uint8, device=dev)
+        b = torch.empty_like(a)
+        fill_us = timeit(lambda: a.fill_(7))
+        copy_us = timeit(lambda: b.copy_(a))
+        rows.append({"MiB": mb, "fill_us": round(fill_us, 2), "fill_GBps": round((mb << 20) / fill_us / 1e3, 1),
+                     "copy_us": round(copy_us, 2), "copy_GBps_read_plus_write": round(2 * (mb << 20) / copy_us / 1e3, 1)})
+        del a, b
+    return {"calibration": "torch fill (write only) and copy (read + write), L2 flushed before each, median of 100",
+            "gpu": torch.cuda.get_device_name(dev), "rows": rows}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -465,6 +517,9 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--num-sms", type=int, default=0)
     ap.add_argument("--unfused", action="store_true", help="time layout and dispatch as two calls")
+    ap.add_argument("--graph", action="store_true", help="replay the step's launches from a CUDA graph")
+    ap.add_argument("--calibrate", action="store_true",
+                    help="print the bandwidth of plain device writes and copies at the step's sizes and exit")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -478,6 +533,9 @@ def main(argv=None):
     rank, local_rank, world = dist_env()
     if world != args.gpus and world > 1:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE {world}")
+    if args.calibrate:
+        print(json.dumps(calibrate(local_rank)), flush=True)
+        return
     line = (run_native if args.impl == "native" else run_reference)(args, rank, local_rank, world)
     if line is not None and rank == 0:
         print(json.dumps(line), flush=True)

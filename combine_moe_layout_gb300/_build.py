@@ -43,16 +43,21 @@ def _inputs_hash(extra: list[str]) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          lib_path: str | None = None) -> str:
+    """Build the library (default: the in-tree _lib/libmoe_layout.so); extra_flags and
+    lib_path build a variant elsewhere without touching the default one."""
     extra = list(extra_flags or [])
-    os.makedirs(LIBDIR, exist_ok=True)
+    lib = lib_path or LIB
+    stamp = lib + ".stamp" if lib_path else STAMP
+    os.makedirs(os.path.dirname(lib), exist_ok=True)
     want = _inputs_hash(extra)
-    if not force and os.path.exists(LIB) and os.path.exists(STAMP):
-        with open(STAMP) as f:
+    if not force and os.path.exists(lib) and os.path.exists(stamp):
+        with open(stamp) as f:
             if f.read().strip() == want:
-                return LIB
+                return lib
     cc = nvcc()
-    objdir = os.path.join(LIBDIR, "obj")
+    objdir = os.path.join(os.path.dirname(lib), "obj" if not lib_path else "obj_" + os.path.basename(lib))
     os.makedirs(objdir, exist_ok=True)
 
     def compile_one(src: str) -> str:
@@ -67,14 +72,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as pool:
         objs = list(pool.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     res = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    with open(STAMP, "w") as f:
+    os.replace(tmp, lib)
+    with open(stamp, "w") as f:
         f.write(want)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -29,6 +29,7 @@ namespace moe {
 
 constexpr int kCombineThreads = 128;
 
+
 struct CombineArgs {
   const uint16_t *y;
   const float *weights;
@@ -36,7 +37,7 @@ struct CombineArgs {
   uint64_t *flags;
   uint16_t *out;
   int32_t *err;
-  int H, k, nflags, chunks;
+  int H, k, nflags, chunks, early;
   int64_t nslots;
 };
 
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
   const int V = a.H / 8;
 
   grid_dependency_wait();
-  grid_dependents_launch();
+  if (a.early) grid_dependents_launch();
   if (b == 0)
     for (int i = threadIdx.x; i < a.nflags; i += blockDim.x) a.flags[i] = 0;
 
@@ -140,17 +141,14 @@ moe_status launch_combine_k(CombineArgs a, int64_t ntok, cudaStream_t stream) {
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  use_pdl(cfg, attr);
   if (cudaLaunchKernelEx(&cfg, combine_kernel<K, VPT>, a) != cudaSuccess) return MOE_ECUDA;
   return launch_status();
 }
 
 moe_status launch_combine(const Sizes &s, const uint16_t *y, const float *weights, const int32_t *tok_slot,
                           uint64_t *flags, uint16_t *out, int32_t *err, cudaStream_t stream) {
-  CombineArgs a{y, weights, tok_slot, flags, out, err, s.H, s.k, s.E * s.R, 1, s.nslots};
+  CombineArgs a{y, weights, tok_slot, flags, out, err, s.H, s.k, s.E * s.R, 1, early_trigger(s.ntok), s.nslots};
   if (s.ntok == 0) {
     // nothing to gather; still clear the flags for the next step
     if (cudaMemsetAsync(flags, 0, static_cast<size_t>(s.E) * s.R * sizeof(uint64_t), stream) != cudaSuccess)

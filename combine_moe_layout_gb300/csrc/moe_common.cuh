@@ -188,6 +188,28 @@ inline moe_status launch_status() { return cudaGetLastError() == cudaSuccess ? M
 // SM count of the current device (queried once per device).
 int sm_count();
 
+// Launch with programmatic dependent launch (MOE_PDL=1): the kernel may be
+// scheduled while the previous kernel in the stream finishes and waits for its
+// results with griddepcontrol.wait.
+#ifndef MOE_PDL
+#define MOE_PDL 1
+#endif
+inline void use_pdl(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[1]) {
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = MOE_PDL;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+}
+
+// Small batches let the next kernel launch as soon as this one has passed its
+// own dependency wait (hiding the next launch behind this kernel); large ones
+// do not, because the next kernel's CTAs would then sit on the SMs for the
+// whole of a long kernel and slow it down.
+#ifndef MOE_EARLY_TRIGGER_TOKENS
+#define MOE_EARLY_TRIGGER_TOKENS 2048
+#endif
+inline int early_trigger(int64_t ntok) { return ntok <= MOE_EARLY_TRIGGER_TOKENS ? 1 : 0; }
+
 // Units issued but not yet consumed when a pipelined loop aborts at unit i:
 // the prologue issued units [0, S), and iteration u >= 1 refilled unit u-1+S,
 // so the loads of units [i, end) may still be in flight.

@@ -35,7 +35,7 @@ struct DispatchArgs {
   float *recv_scales;
   int4 *recv_meta;
   int32_t *err;
-  int R, T, k, max_m, nsc, stages, pieces;
+  int R, T, k, max_m, nsc, stages, pieces, early;
   uint32_t row_bytes, piece_bytes;
   int64_t nslots, nunits;
 };
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(32) dispatch_kernel(DispatchArgs a) {
     for (int64_t i = 0; i < n_mine && i < S; ++i)
       issue_unit_load(a, dsm + static_cast<size_t>(i) * a.piece_bytes, &full[i], first + i * stride);
   grid_dependency_wait();
-  grid_dependents_launch();
+  if (a.early) grid_dependents_launch();
 
   int64_t i = 0;
   for (; i < n_mine; ++i) {
@@ -169,6 +169,7 @@ moe_status launch_dispatch(const Sizes &s, const void *x, const float *x_scales,
   a.k = s.k;
   a.max_m = s.max_m;
   a.nsc = s.nsc;
+  a.early = early_trigger(s.ntok);
   a.row_bytes = static_cast<uint32_t>(s.row_bytes);
   a.piece_bytes = a.row_bytes < kPieceMax ? a.row_bytes : kPieceMax;
   a.pieces = static_cast<int>((a.row_bytes + a.piece_bytes - 1) / a.piece_bytes);
@@ -193,10 +194,7 @@ moe_status launch_dispatch(const Sizes &s, const void *x, const float *x_scales,
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  use_pdl(cfg, attr);
   if (cudaLaunchKernelEx(&cfg, dispatch_kernel, a) != cudaSuccess) return MOE_ECUDA;
   return launch_status();
 }

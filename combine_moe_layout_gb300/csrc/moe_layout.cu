@@ -22,9 +22,19 @@
 //      see them once this grid completes (griddepcontrol.wait under
 //      programmatic dependent launch), so plain stores suffice: a release fence
 //      per flag would only lengthen this latency-bound kernel.
-#include <cstdio>
+//
+// Large batches (more than 128 tokens per rank) use a thread-block cluster per
+// source rank instead: CTA r of the cluster owns tokens [r*TPC, (r+1)*TPC),
+// builds the bitmaps of its slice, publishes its per-expert counts in its own
+// shared memory, and after a cluster barrier sums the counts of CTAs 0..r-1
+// through distributed shared memory to get its bases. Every entry is counted
+// once, with no global scratch and no grid-wide step; the last CTA of the
+// cluster writes the totals.
+#include <cooperative_groups.h>
 
 #include "moe_common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace moe {
 
@@ -39,7 +49,7 @@ struct LayoutArgs {
   uint64_t *flags;
   int32_t *tok_slot;
   int32_t *err;
-  int R, T, E, k, max_m;
+  int R, T, E, k, max_m, early;
 };
 
 __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
@@ -53,7 +63,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
 
   grid_dependency_wait();
-  grid_dependents_launch();  // dispatch may start loading its rows meanwhile
+  if (a.early) grid_dependents_launch();  // dispatch may start loading its rows meanwhile
   for (int i = tid; i < a.E * (1 + kLayoutWords); i += blockDim.x) lsm[i] = 0;
   __syncthreads();
 
@@ -120,6 +130,97 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
   }
 }
 
+constexpr int kClusterMax = 8;             // portable cluster size
+constexpr int kClusterThreads = 512;
+constexpr int kClusterTokensPerCta = 512;
+constexpr size_t kClusterMaxSmem = 200 * 1024;
+
+__global__ void __launch_bounds__(kClusterThreads) layout_cluster_kernel(LayoutArgs a, int tpc, int words) {
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ uint32_t csm[];
+  uint32_t *bits = csm;                                           // [E][words]
+  int32_t *hist = reinterpret_cast<int32_t *>(csm + a.E * words);  // [E] counts of this slice
+  int32_t *base = hist + a.E;                                     // [E] counts of the earlier slices
+  const int r = static_cast<int>(cluster.block_rank());
+  const int csize = static_cast<int>(cluster.num_blocks());
+  const int src = blockIdx.y;
+  const int t0 = r * tpc;
+  const int tn = max(0, min(tpc, a.T - t0));
+  const int tid = threadIdx.x;
+
+  grid_dependency_wait();
+  if (a.early) grid_dependents_launch();
+  for (int i = tid; i < a.E * words; i += blockDim.x) bits[i] = 0;
+  __syncthreads();
+
+  const int32_t *own = a.topk_idx + (static_cast<int64_t>(src) * a.T + t0) * a.k;
+  const int n_own = tn * a.k;
+  for (int i = tid; i < n_own; i += blockDim.x) {
+    const int e = __ldg(own + i);
+    if (e < 0 || e >= a.E) {
+      latch_error(a.err, MOE_EINVAL);
+      continue;
+    }
+    const int tl = i / a.k;
+    const uint32_t bit = 1u << (tl & 31);
+    if (atomicOr(&bits[e * words + (tl >> 5)], bit) & bit) latch_error(a.err, MOE_EINVAL);
+  }
+  __syncthreads();
+  for (int e = tid; e < a.E; e += blockDim.x) {
+    int c = 0;
+    for (int w = 0; w < words; ++w) c += __popc(bits[e * words + w]);
+    hist[e] = c;
+  }
+  cluster.sync();  // every slice's counts are visible to the whole cluster
+
+  for (int e = tid; e < a.E; e += blockDim.x) {
+    int b = 0;
+    for (int q = 0; q < r; ++q) b += *cluster.map_shared_rank(hist + e, q);
+    base[e] = b;
+    if (r == csize - 1) {
+      const int c = b + hist[e];
+      const int64_t reg = static_cast<int64_t>(e) * a.R + src;
+      a.counts[reg] = c;
+      a.flags[reg] = static_cast<uint64_t>(c) + 1;
+    }
+  }
+  __syncthreads();
+
+  int32_t *out = a.tok_slot + (static_cast<int64_t>(src) * a.T + t0) * a.k;
+  for (int i = tid; i < n_own; i += blockDim.x) {
+    const int e = __ldg(own + i);
+    int32_t slot = -1;
+    if (e >= 0 && e < a.E) {
+      const int tl = i / a.k;
+      const uint32_t *b = bits + e * words;
+      int pos = base[e];
+      for (int w = 0; w < (tl >> 5); ++w) pos += __popc(b[w]);
+      pos += __popc(b[tl >> 5] & ((1u << (tl & 31)) - 1u));
+      if (pos < a.max_m)
+        slot = static_cast<int32_t>((static_cast<int64_t>(e) * a.R + src) * a.max_m + pos);
+      else
+        latch_error(a.err, MOE_EOVERFLOW);
+    }
+    out[i] = slot;
+  }
+  cluster.sync();  // no CTA leaves while another may still read its counts
+}
+
+// Cluster shape for a batch, or false when the chunked kernel must be used.
+static bool cluster_shape(const Sizes &s, int *csize, int *tpc, int *words, size_t *smem) {
+  if (s.T <= kLayoutChunk) return false;
+  int c = (s.T + kClusterTokensPerCta - 1) / kClusterTokensPerCta;
+  if (c > kClusterMax) c = kClusterMax;
+  if (c < 1) c = 1;
+  int per = (s.T + c - 1) / c;
+  per = (per + 31) / 32 * 32;
+  *csize = c;
+  *tpc = per;
+  *words = per / 32;
+  *smem = (static_cast<size_t>(s.E) * *words + 2 * static_cast<size_t>(s.E)) * sizeof(uint32_t);
+  return *smem <= kClusterMaxSmem;
+}
+
 int sm_count() {
   static int cache[64] = {0};
   int dev = 0;
@@ -134,7 +235,30 @@ int sm_count() {
 moe_status launch_layout(const Sizes &s, const int32_t *topk_idx, int32_t *counts, uint64_t *flags,
                          int32_t *tok_slot, int32_t *err, cudaStream_t stream) {
   if (s.E > kLayoutMaxExperts) return MOE_EINVAL;
-  LayoutArgs a{topk_idx, counts, flags, tok_slot, err, s.R, s.T, s.E, s.k, s.max_m};
+  LayoutArgs a{topk_idx, counts, flags, tok_slot, err, s.R, s.T, s.E, s.k, s.max_m, early_trigger(s.ntok)};
+  int csize = 0, tpc = 0, words = 0;
+  size_t csmem = 0;
+  if (cluster_shape(s, &csize, &tpc, &words, &csmem)) {
+    if (csmem > 48 * 1024 && cudaFuncSetAttribute(layout_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  static_cast<int>(csmem)) != cudaSuccess)
+      return MOE_ECUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(csize, s.R, 1);
+    cfg.blockDim = dim3(kClusterThreads, 1, 1);
+    cfg.dynamicSmemBytes = csmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = MOE_PDL;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = csize;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, layout_cluster_kernel, a, tpc, words) != cudaSuccess) return MOE_ECUDA;
+    return launch_status();
+  }
   const size_t smem = static_cast<size_t>(s.E) * (1 + kLayoutWords) * sizeof(uint32_t);
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
@@ -147,10 +271,7 @@ moe_status launch_layout(const Sizes &s, const int32_t *topk_idx, int32_t *count
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  use_pdl(cfg, attr);
   if (cudaLaunchKernelEx(&cfg, layout_kernel, a) != cudaSuccess) return MOE_ECUDA;
   return launch_status();
 }

@@ -38,7 +38,7 @@ struct FusedArgs {
   float *recv_scales;
   int4 *recv_meta;
   int32_t *err;
-  int R, T, E, k, max_m, nsc, words, ctas_per_rank, stages;
+  int R, T, E, k, max_m, nsc, words, ctas_per_rank, stages, early;
   uint32_t row_bytes;
   int64_t nslots;
 };
@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
     }
   }
   grid_dependency_wait();
-  grid_dependents_launch();
+  if (a.early) grid_dependents_launch();
 
   // per-expert token bitmaps of the whole source rank
   for (int i = tid; i < a.E * a.words; i += kFusedThreads) bits[i] = 0;
@@ -204,6 +204,7 @@ moe_status launch_layout_dispatch(const Sizes &s, const int32_t *topk_idx, const
   a.max_m = s.max_m;
   a.nsc = s.nsc;
   a.words = (s.T + 31) / 32;
+  a.early = early_trigger(s.ntok);
   a.row_bytes = static_cast<uint32_t>(s.row_bytes);
   a.nslots = s.nslots;
 
@@ -233,10 +234,7 @@ moe_status launch_layout_dispatch(const Sizes &s, const int32_t *topk_idx, const
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    use_pdl(cfg, attr);
     if (cudaLaunchKernelEx(&cfg, layout_dispatch_kernel, a) != cudaSuccess) return MOE_ECUDA;
     return launch_status();
   }
