@@ -165,6 +165,11 @@ EDGE = {
     "k6_bf16": dict(num_ranks=4, tokens_per_rank=77, hidden=1024, num_experts=16, topk=6, max_m=80),
     # layout on a cluster of 3 CTAs per rank, the last slice ragged
     "cluster3_ragged": dict(num_ranks=2, tokens_per_rank=1500, hidden=64, num_experts=32, topk=4, max_m=1500),
+    # 16384 tokens and k >= 4: combine stages its pieces with bulk TMA; hidden 256 leaves a partial chunk
+    "tma_combine_k6_bf16": dict(num_ranks=4, tokens_per_rank=4096, hidden=256, num_experts=16, topk=6,
+                                max_m=4096, x_dist="normal"),
+    "tma_combine_k4_fp8": dict(num_ranks=8, tokens_per_rank=2048, hidden=1024, num_experts=32, topk=4,
+                               max_m=2048, dtype="fp8", expert="scale", x_dist="normal", renormalize=False),
     # 4096 experts: the cluster's bitmaps do not fit, the chunked layout kernel runs
     "many_experts_chunked": dict(num_ranks=1, tokens_per_rank=1024, hidden=64, num_experts=4096, topk=2,
                                  max_m=1024),
