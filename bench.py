@@ -504,8 +504,19 @@ def calibrate(local_rank: int) -> dict:
         rows.append({"MiB": mb, "fill_us": round(fill_us, 2), "fill_GBps": round((mb << 20) / fill_us / 1e3, 1),
                      "copy_us": round(copy_us, 2), "copy_GBps_read_plus_write": round(2 * (mb << 20) / copy_us / 1e3, 1)})
         del a, b
-    return {"calibration": "torch fill (write only) and copy (read + write), L2 flushed before each, median of 100",
-            "gpu": torch.cuda.get_device_name(dev), "rows": rows}
+    host = []
+    for mb in (7.5, 15, 60, 240):
+        n = int(mb * (1 << 20))
+        h = torch.empty(n, dtype=torch.uint8).pin_memory()
+        dd = torch.empty(n, dtype=torch.uint8, device=dev)
+        h2d_us = timeit(lambda: dd.copy_(h, non_blocking=True), 50)
+        d2h_us = timeit(lambda: h.copy_(dd, non_blocking=True), 50)
+        host.append({"MiB": mb, "h2d_us": round(h2d_us, 2), "h2d_GBps": round(n / h2d_us / 1e3, 1),
+                     "d2h_us": round(d2h_us, 2), "d2h_GBps": round(n / d2h_us / 1e3, 1)})
+        del h, dd
+    return {"calibration": "torch fill (write only) and copy (read + write), L2 flushed before each, median of 100; "
+                           "pinned host <-> device copies, median of 50",
+            "gpu": torch.cuda.get_device_name(dev), "rows": rows, "host_copies": host}
 
 
 def main(argv=None):
