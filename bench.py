@@ -216,13 +216,13 @@ def run_native(args, rank, local_rank, world):
     fused = not args.unfused
     kernels = B.moe_layout_dispatch_kernels(step.desc) + 1 if fused else 3
 
-    def path(dd):
+    def path(dd, out=None):
         if fused:
             step.layout_dispatch(dd)
         else:
             step.layout(dd)
             step.dispatch(dd)
-        step.combine(dd)
+        step.combine(dd, out=out)
 
     K, W = args.steps, args.warmup
     for _ in range(W):
@@ -288,29 +288,47 @@ def run_native(args, rank, local_rank, world):
             hpack[off:off + a_.size].copy_(torch.from_numpy(a_))
         dpack = torch.empty(o, dtype=torch.uint8, device=dev)
 
-        def view(i_, dtype, shape):
+        def view(pack, i_, dtype, shape):
             n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
-            return dpack[offs[i_]:offs[i_] + n].view(dtype).view(shape)
+            return pack[offs[i_]:offs[i_] + n].view(dtype).view(shape)
 
-        R_, T_, H_, k_ = w.num_ranks, w.tokens_per_rank, w.hidden, w.topk
-        dx = view(0, torch.uint8 if w.dtype == "fp8" else torch.bfloat16, (R_, T_, H_))
-        d2 = P.DeviceInputs(view(1, torch.int32, (R_, T_, k_)), view(2, torch.float32, (R_, T_, k_)), dx,
-                            view(3, torch.float32, (R_, T_, H_ // 128)) if inp.x_scales is not None else None)
+        def inputs_in(pack):
+            R_, T_, H_, k_ = w.num_ranks, w.tokens_per_rank, w.hidden, w.topk
+            xx = view(pack, 0, torch.uint8 if w.dtype == "fp8" else torch.bfloat16, (R_, T_, H_))
+            return P.DeviceInputs(view(pack, 1, torch.int32, (R_, T_, k_)), view(pack, 2, torch.float32, (R_, T_, k_)),
+                                  xx, view(pack, 3, torch.float32, (R_, T_, H_ // 128))
+                                  if inp.x_scales is not None else None)
+
         hout = torch.empty((w.num_tokens, w.hidden), dtype=torch.bfloat16).pin_memory()
         out_view = step.buf.out.view(w.num_tokens, w.hidden)
         eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-        for i in range(K):
-            flush()
-            eev[i][0].record(stream)
-            dpack.copy_(hpack, non_blocking=True)
-            path(d2)
-            hout.copy_(out_view, non_blocking=True)
-            eev[i][1].record(stream)
+        if args.e2e_mode == "copy":
+            d2 = inputs_in(dpack)
+            for i in range(K):
+                flush()
+                eev[i][0].record(stream)
+                dpack.copy_(hpack, non_blocking=True)
+                path(d2)
+                hout.copy_(out_view, non_blocking=True)
+                eev[i][1].record(stream)
+            how = "one pinned H2D copy of the packed inputs, one D2H copy of the bf16 output"
+        else:
+            h2 = inputs_in(hpack)
+            hout_steps = hout.view(w.num_ranks, w.tokens_per_rank, w.hidden)
+            for i in range(K):
+                flush()
+                eev[i][0].record(stream)
+                path(h2, out=hout_steps)
+                eev[i][1].record(stream)
+            how = ("zero-copy: the kernels read the packed inputs from pinned host memory and write the bf16 "
+                   "output into pinned host memory over NVLink-C2C, no separate copies")
         torch.cuda.synchronize()
         e2e_ms = sum(a.elapsed_time(b) for a, b in eev)
         e2e = {"value": None, "unit": "tokens/s", "h2d_bytes_per_step": int(sum(a_.size for a_ in parts)),
-               "d2h_bytes_per_step": hout.numel() * 2, "local_ms_total": e2e_ms,
-               "copies": "one pinned H2D copy of the packed inputs, one D2H copy of the bf16 output"}
+               "d2h_bytes_per_step": hout.numel() * 2, "local_ms_total": e2e_ms, "copies": how}
+        if args.e2e_mode != "copy":
+            path(d)  # the same step on device buffers, to compare
+            torch.cuda.synchronize()
         if not torch.equal(hout.view(torch.int16), out_view.cpu().view(torch.int16)):
             raise RuntimeError("end-to-end output differs from the device output")
 
@@ -532,6 +550,8 @@ def main(argv=None):
     ap.add_argument("--calibrate", action="store_true",
                     help="print the bandwidth of plain device writes and copies at the step's sizes and exit")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-mode", choices=("zero-copy", "copy"), default="zero-copy",
+                    help="end to end: kernels read/write pinned host memory directly, or copy engines move the data")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)

@@ -82,11 +82,13 @@ def load():
     return lib
 
 
-def _ptr(t: torch.Tensor | None):
+def _ptr(t: torch.Tensor | None, host_ok: bool = False):
+    """Device pointer of a tensor; host_ok also admits pinned host memory (the
+    step's inputs and output, which the kernels can read and write directly)."""
     if t is None:
         return None
-    if not t.is_cuda:
-        raise ValueError("libmoe_layout takes device tensors")
+    if not (t.is_cuda or (host_ok and t.is_pinned())):
+        raise ValueError("libmoe_layout takes device tensors" + (" or pinned host tensors" if host_ok else ""))
     if not t.is_contiguous():
         raise ValueError("libmoe_layout takes contiguous tensors")
     return ctypes.c_void_p(t.data_ptr())
@@ -113,19 +115,20 @@ def moe_buffer_sizes(desc: MoeDesc) -> dict:
 
 
 def moe_layout(desc, topk_idx, counts, flags, tok_slot, err, stream=None):
-    _check(load().moe_layout(ctypes.byref(desc), _ptr(topk_idx), _ptr(counts), _ptr(flags), _ptr(tok_slot),
+    _check(load().moe_layout(ctypes.byref(desc), _ptr(topk_idx, True), _ptr(counts), _ptr(flags), _ptr(tok_slot),
                              _ptr(err), _stream(stream)), "moe_layout")
 
 
 def moe_dispatch(desc, x, x_scales, tok_slot, flags, recv_x, recv_scales, recv_meta, err, stream=None):
-    _check(load().moe_dispatch(ctypes.byref(desc), _ptr(x), _ptr(x_scales), _ptr(tok_slot), _ptr(flags),
+    _check(load().moe_dispatch(ctypes.byref(desc), _ptr(x, True), _ptr(x_scales, True), _ptr(tok_slot), _ptr(flags),
                                _ptr(recv_x), _ptr(recv_scales), _ptr(recv_meta), _ptr(err), _stream(stream)),
            "moe_dispatch")
 
 
 def moe_layout_dispatch(desc, topk_idx, x, x_scales, counts, flags, tok_slot, recv_x, recv_scales, recv_meta, err,
                         stream=None):
-    _check(load().moe_layout_dispatch(ctypes.byref(desc), _ptr(topk_idx), _ptr(x), _ptr(x_scales), _ptr(counts),
+    _check(load().moe_layout_dispatch(ctypes.byref(desc), _ptr(topk_idx, True), _ptr(x, True), _ptr(x_scales, True),
+                                      _ptr(counts),
                                       _ptr(flags), _ptr(tok_slot), _ptr(recv_x), _ptr(recv_scales), _ptr(recv_meta),
                                       _ptr(err), _stream(stream)), "moe_layout_dispatch")
 
@@ -142,8 +145,8 @@ def moe_expert_stub(desc, recv_x, recv_scales, counts, expert_out, err, stream=N
 
 
 def moe_combine(desc, expert_out, topk_weights, tok_slot, flags, out, err, stream=None):
-    _check(load().moe_combine(ctypes.byref(desc), _ptr(expert_out), _ptr(topk_weights), _ptr(tok_slot),
-                              _ptr(flags), _ptr(out), _ptr(err), _stream(stream)), "moe_combine")
+    _check(load().moe_combine(ctypes.byref(desc), _ptr(expert_out), _ptr(topk_weights, True), _ptr(tok_slot),
+                              _ptr(flags), _ptr(out, True), _ptr(err), _stream(stream)), "moe_combine")
 
 
 def moe_reset(desc, flags, err, stream=None):

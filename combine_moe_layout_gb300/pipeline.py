@@ -23,6 +23,19 @@ class DeviceInputs:
     x_scales: torch.Tensor | None
 
 
+def to_pinned_host(inputs) -> DeviceInputs:
+    """The generated inputs in pinned host memory, for kernels that read them
+    directly over the CPU-GPU link (bf16 bits are reinterpreted, not converted)."""
+    def t(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+
+    x = t(inputs.x)
+    if x.dtype == torch.uint16:
+        x = x.view(torch.bfloat16)
+    return DeviceInputs(t(inputs.topk_idx), t(inputs.topk_weights), x,
+                        None if inputs.x_scales is None else t(inputs.x_scales))
+
+
 def to_device(inputs, device, pin: bool = False) -> DeviceInputs:
     """Copy generated numpy inputs to the device (bf16 bits are reinterpreted, not converted)."""
     def t(a):
@@ -75,9 +88,11 @@ class MoeStep:
             b = self.buf
             B.moe_expert_stub(self.desc, b.recv_x, b.recv_scales, b.counts, b.expert_out, b.err, stream)
 
-    def combine(self, d: DeviceInputs, stream=None):
+    def combine(self, d: DeviceInputs, stream=None, out=None):
+        """out: the step's output buffer (default: the device buffer; may be pinned host memory)."""
         b = self.buf
-        B.moe_combine(self.desc, self.y, d.topk_weights, b.tok_slot, b.flags, b.out, b.err, stream)
+        B.moe_combine(self.desc, self.y, d.topk_weights, b.tok_slot, b.flags, b.out if out is None else out, b.err,
+                      stream)
 
     def run(self, d: DeviceInputs, stream=None, fused: bool = False):
         if fused:

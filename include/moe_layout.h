@@ -28,6 +28,12 @@
  *   - Pointers are device pointers unless stated; the caller allocates every
  *     buffer (moe_buffer_sizes gives the sizes) and the library allocates
  *     nothing and keeps no state between calls.
+ *   - The step's inputs (topk_idx, x, x_scales, topk_weights) and its output
+ *     (out) may instead be pinned host memory (cudaHostAlloc or
+ *     cudaHostRegister, with unified addressing): the kernels then read and
+ *     write them directly over the CPU-GPU link, which on Grace-based systems
+ *     replaces separate host<->device copies. Every other buffer must be
+ *     device memory.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
  *     asynchronous on it and never synchronise with the host, except
  *     moe_get_error.

@@ -320,3 +320,33 @@ def test_host_validation():
     with pytest.raises(B.MoeError):
         B.moe_dispatch(B.MoeDesc.of(w), xs, None, step.buf.tok_slot, step.buf.flags, step.buf.recv_x, None,
                        step.buf.recv_meta, step.buf.err)
+
+
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+@pytest.mark.parametrize("name", ["tiny", "ds_decode", "skewed"])
+def test_pinned_host_inputs_and_output(name, fused):
+    """Inputs and output in pinned host memory, read and written by the kernels
+    directly: the same bits as the all-device step."""
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w)
+    step = P.MoeStep(w, "cuda:0")
+    d = P.to_device(inp, "cuda:0")
+    step.reset()
+    step.run(d, fused=fused)
+    assert step.error() == B.MOE_OK
+    ref = step.buf.out.clone()
+    ref_meta = step.buf.recv_meta.clone()
+    h = P.to_pinned_host(inp)
+    hout = torch.empty((w.num_ranks, w.tokens_per_rank, w.hidden), dtype=torch.bfloat16).pin_memory()
+    step.buf.recv_meta.fill_(-7)
+    if fused:
+        step.layout_dispatch(h)
+    else:
+        step.layout(h)
+        step.dispatch(h)
+    step.experts()
+    step.combine(h, out=hout)
+    assert step.error() == B.MOE_OK
+    torch.cuda.synchronize()
+    assert torch.equal(hout.view(torch.int16), ref.cpu().view(torch.int16))
+    assert torch.equal(step.buf.recv_meta, ref_meta)
