@@ -332,6 +332,7 @@ def test_pinned_host_inputs_and_output(name, fused):
     step = P.MoeStep(w, "cuda:0")
     d = P.to_device(inp, "cuda:0")
     step.reset()
+    step.buf.recv_meta.fill_(-7)
     step.run(d, fused=fused)
     assert step.error() == B.MOE_OK
     ref = step.buf.out.clone()
