@@ -35,7 +35,7 @@ class Workload:
     num_experts: int        # E
     topk: int               # k
     max_m: int              # slots per (expert, source rank)
-    dtype: str              # "bf16" or "fp8"
+    dtype: str              # "bf16", "fp8", or "bf16q" (bf16 rows quantised to fp8 on dispatch)
     router: str             # "softmax", "zipf" or "group"
     renormalize: bool       # softmax router: renormalise the k weights to sum 1
     expert: str             # "identity" or "scale" (y = x * (1 + e/256))
@@ -52,29 +52,36 @@ class Workload:
 
     @property
     def row_bytes(self) -> int:
+        """Bytes of a dispatched row (what a slot holds)."""
+        return 2 * self.hidden if self.dtype == "bf16" else self.hidden
+
+    @property
+    def in_row_bytes(self) -> int:
+        """Bytes of a caller's input row."""
         return self.hidden if self.dtype == "fp8" else 2 * self.hidden
 
     @property
     def scales_per_row(self) -> int:
-        return self.hidden // SCALE_BLOCK if self.dtype == "fp8" else 0
+        return 0 if self.dtype == "bf16" else self.hidden // SCALE_BLOCK
 
     @property
     def dtype_code(self) -> int:
-        return 1 if self.dtype == "fp8" else 0
+        return {"bf16": 0, "fp8": 1, "bf16q": 2}[self.dtype]
 
     def algorithmic_bytes(self) -> dict:
         """Bytes each step must move at least once (slots never touched are not counted).
 
         layout: read topk_idx, write tok_slot, write counts and flags.
-        dispatch: read every row (+ scales) once, write it (+ scales + 16-byte
-        header) into k slots, read tok_slot.
+        dispatch: read every input row (+ its scales) once, write the dispatched
+        row (+ scales + 16-byte header) into k slots, read tok_slot.
         combine: read k bf16 expert rows per token, write one bf16 row, read
         weights and tok_slot.
         """
         N, k, H, E, R = self.num_tokens, self.topk, self.hidden, self.num_experts, self.num_ranks
         sc = self.scales_per_row * 4
         lay = N * k * 4 + N * k * 4 + E * R * (4 + 8)
-        dis = N * (self.row_bytes + sc) + N * k * (self.row_bytes + sc + 16) + N * k * 4
+        in_sc = sc if self.dtype == "fp8" else 0
+        dis = N * (self.in_row_bytes + in_sc) + N * k * (self.row_bytes + sc + 16) + N * k * 4
         com = N * k * 2 * H + N * 2 * H + N * k * 4 + N * k * 4
         return {"layout": lay, "dispatch": dis, "combine": com, "total": lay + dis + com}
 
@@ -85,6 +92,9 @@ WORKLOADS = {
     "mixtral": Workload("mixtral", 8, 4096, 4096, 8, 2, 4096, "bf16", "softmax", True, "identity", "normal"),
     "skewed": Workload("skewed", 16, 256, 7168, 256, 8, 256, "bf16", "zipf", True, "identity", "normal"),
     "ds_prefill": Workload("ds_prefill", 8, 4096, 7168, 256, 8, 4096, "fp8", "group", True, "scale", "normal"),
+    # the decode shape with bf16 rows quantised to fp8 + scales on dispatch
+    "ds_decode_bf16in": Workload("ds_decode_bf16in", 8, 128, 7168, 256, 8, 128, "bf16q", "softmax", False, "scale",
+                                 "normal"),
 }
 
 DESCRIPTIONS = {
@@ -96,6 +106,8 @@ DESCRIPTIONS = {
     "skewed": "Zipf(1.2) routing: 16 ranks x 256 tokens, hidden 7168 bf16, 256 experts, top-8, max_m 256",
     "ds_prefill": "DeepSeek-shape prefill: 8 ranks x 4096 tokens, hidden 7168 fp8 e4m3 + scales, 256 experts in "
                   "8 groups, top-4 groups then top-8 of sigmoid scores, max_m 4096",
+    "ds_decode_bf16in": "DeepSeek-shape decode with bf16 input rows quantised on dispatch to fp8 e4m3 + 128-elt "
+                        "fp32 scales: 8 ranks x 128 tokens, hidden 7168, 256 experts, top-8 of softmax, max_m 128",
 }
 
 
@@ -108,8 +120,8 @@ def custom(name="custom", **kw) -> Workload:
 class Inputs:
     topk_idx: np.ndarray      # [R][T][k] int32
     topk_weights: np.ndarray  # [R][T][k] float32
-    x: np.ndarray             # [R][T][H] uint16 bf16 bits, or uint8 e4m3 codes
-    x_scales: np.ndarray | None  # [R][T][H/128] float32 (fp8 only)
+    x: np.ndarray             # [R][T][H] uint16 bf16 bits (bf16, bf16q), or uint8 e4m3 codes (fp8)
+    x_scales: np.ndarray | None  # [R][T][H/128] float32 (fp8 input only)
 
 
 # --- routers (input generation only) -----------------------------------------

@@ -41,7 +41,7 @@ _STAMP = os.path.join(_LIBDIR, "liboracle.stamp")
 _CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared"]
 
 OK, EINVAL, EOVERFLOW = 0, -1, -2
-BF16, FP8_E4M3 = 0, 1
+BF16, FP8_E4M3, BF16_TO_FP8 = 0, 1, 2
 
 _lib = None
 
@@ -80,6 +80,10 @@ def _bind(path: str):
     lib.orc_bf16_from_double.restype = ctypes.c_uint16
     lib.orc_e4m3_value.argtypes = [ctypes.c_uint8]
     lib.orc_e4m3_value.restype = dbl
+    lib.orc_e4m3_from_float.argtypes = [ctypes.c_float]
+    lib.orc_e4m3_from_float.restype = ctypes.c_uint8
+    lib.orc_quantize_row.argtypes = [vp, i32, vp, vp]
+    lib.orc_quantize_row.restype = None
     lib.orc_validate.argtypes = [i32] * 7
     lib.orc_validate.restype = i32
     lib.orc_buffer_sizes.argtypes = [i32] * 7 + [vp]
@@ -149,6 +153,20 @@ def e4m3_value(code: int) -> float:
     return _load().orc_e4m3_value(int(code))
 
 
+def e4m3_from_float(v: float) -> int:
+    return int(_load().orc_e4m3_from_float(float(v)))
+
+
+def quantize_row(x_bits: np.ndarray):
+    """E4M3 codes and 128-element fp32 scales of one bf16 row (uint16 bits)."""
+    xb = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    H = xb.size
+    q = np.zeros(H, np.uint8)
+    sc = np.zeros(H // 128, np.float32)
+    _load().orc_quantize_row(_p(xb), H, _p(q), _p(sc))
+    return q, sc
+
+
 # --- problem description ----------------------------------------------------
 
 def validate(R, T, H, E, k, max_m, dtype) -> int:
@@ -193,9 +211,10 @@ def dispatch(x: np.ndarray, x_scales, tok_slot: np.ndarray, num_experts: int, ma
     """Slots written for the selected tokens (flat ids src*T+t; all tokens when None)."""
     R, T, k = tok_slot.shape
     H = x.shape[-1]  # x is [R][T][H] of uint8 codes (fp8) or uint16 bits (bf16)
-    row_bytes = H if dtype == FP8_E4M3 else 2 * H
-    xb = np.ascontiguousarray(x).view(np.uint8).reshape(R * T, row_bytes)
-    nsc = H // 128 if dtype == FP8_E4M3 else 0
+    row_bytes = 2 * H if dtype == BF16 else H  # bytes of a dispatched row
+    in_row_bytes = H if dtype == FP8_E4M3 else 2 * H
+    xb = np.ascontiguousarray(x).view(np.uint8).reshape(R * T, in_row_bytes)
+    nsc = 0 if dtype == BF16 else H // 128
     sc = None
     if dtype == FP8_E4M3:
         sc = np.ascontiguousarray(x_scales, dtype=np.float32).reshape(R * T, nsc)
@@ -253,7 +272,7 @@ class OracleResult:
 def run(workload, inputs, sel: np.ndarray | None = None) -> OracleResult:
     """Layout (all tokens), then dispatch, synthetic experts and combine for the selected tokens."""
     w = workload
-    dt = FP8_E4M3 if w.dtype == "fp8" else BF16
+    dt = w.dtype_code
     counts, flags, tok_slot = layout(inputs.topk_idx, w.num_experts, w.max_m)
     if sel is None:
         sel = np.arange(w.num_ranks * w.tokens_per_rank, dtype=np.int64)

@@ -45,7 +45,9 @@ enum {
   ORC_EOVERFLOW = -2,
 };
 
-enum { ORC_BF16 = 0, ORC_FP8_E4M3 = 1 };
+/* Dispatched row formats. ORC_BF16_TO_FP8: the caller's rows are bf16 and
+ * dispatch quantises them to E4M3 with 128-element fp32 scales on the way. */
+enum { ORC_BF16 = 0, ORC_FP8_E4M3 = 1, ORC_BF16_TO_FP8 = 2 };
 
 /* ------------------------------------------------------------------------ */
 /* Number formats, from their definitions.                                   */
@@ -108,7 +110,7 @@ int orc_validate(int R, int T, int H, int E, int k, int max_m, int dtype) {
   if (E % R != 0) return ORC_EINVAL;       /* num_experts // EP must be exact */
   if (k > E) return ORC_EINVAL;
   if (T > max_m) return ORC_EINVAL;        /* max_m bounds tokens per rank */
-  if (dtype == ORC_FP8_E4M3) {
+  if (dtype == ORC_FP8_E4M3 || dtype == ORC_BF16_TO_FP8) {
     if (H % 128 != 0) return ORC_EINVAL;   /* one scale per 128 elements */
   } else if (dtype == ORC_BF16) {
     if (H % 8 != 0) return ORC_EINVAL;     /* rows of whole 16-byte vectors */
@@ -120,12 +122,60 @@ int orc_validate(int R, int T, int H, int E, int k, int max_m, int dtype) {
   return ORC_OK;
 }
 
+/* Bytes of a dispatched row (in the slots) and of a caller's input row. */
 static int64_t orc_row_bytes(int H, int dtype) {
+  return dtype == ORC_BF16 ? (int64_t)2 * H : (int64_t)H;
+}
+
+static int64_t orc_in_row_bytes(int H, int dtype) {
   return dtype == ORC_FP8_E4M3 ? (int64_t)H : (int64_t)2 * H;
 }
 
 static int64_t orc_scale_count(int H, int dtype) {
-  return dtype == ORC_FP8_E4M3 ? (int64_t)H / 128 : 0;
+  return dtype == ORC_BF16 ? 0 : (int64_t)H / 128;
+}
+
+/* Nearest FP8 E4M3 ("e4m3fn") code to a float, ties to even; magnitudes
+ * beyond the largest finite value (448) saturate to +-448, since the format
+ * has no infinity; NaN stays NaN. The representable magnitudes are m * 2^-9
+ * (m = 0..7, subnormal) and (8 + m) * 2^(E - 10) for E = 1..15, except
+ * E = 15, m = 7 (NaN); in the binade [2^e, 2^(e+1)) they are spaced 2^(e-3),
+ * and below 2^-6 the spacing stays 2^-9. */
+uint8_t orc_e4m3_from_float(float f) {
+  if (f != f) return 0x7F;
+  uint8_t sign = signbit(f) ? 0x80 : 0;
+  double a = fabs((double)f);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+  if (a == 0.0) return sign;
+  int e = ilogb(a);
+  if (e < -6) e = -6;
+  double quantum = scalbn(1.0, e - 3);
+  double r = rint(a / quantum) * quantum;
+  if (r < 0x1p-6) return (uint8_t)(sign | (uint8_t)(r / 0x1p-9)); /* subnormal */
+  int E = ilogb(r);
+  int m = (int)(r / scalbn(1.0, E - 3)) - 8;
+  return (uint8_t)(sign | ((E + 7) << 3) | m);
+}
+
+/* Block quantisation of one bf16 row to E4M3 with one fp32 scale per 128
+ * contiguous elements ("NVSHMEM and DeepEP", high-throughput section: FP8
+ * dispatch with fine-grained 128-element scales). The decision of each code
+ * is taken in fp32, as a GPU does it: scale = amax / 448 (1 for an all-zero
+ * block), code = e4m3(x / scale) with IEEE fp32 division. */
+void orc_quantize_row(const uint16_t *x, int H, uint8_t *q, float *scales) {
+  for (int b = 0; b < H / 128; ++b) {
+    float amax = 0.0f;
+    for (int h = b * 128; h < (b + 1) * 128; ++h) {
+      float v = fabsf((float)orc_bf16_value(x[h]));
+      if (v > amax) amax = v;
+    }
+    float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    scales[b] = s;
+    for (int h = b * 128; h < (b + 1) * 128; ++h) {
+      float v = (float)orc_bf16_value(x[h]);
+      q[h] = orc_e4m3_from_float(v / s);
+    }
+  }
 }
 
 /* Bytes of every buffer of the path for the whole allocation (all R logical
@@ -200,29 +250,56 @@ int orc_dispatch(int R, int T, int H, int E, int k, int max_m, int dtype,
                  int64_t n_sel, const int64_t *sel, int64_t *slot_id,
                  uint8_t *rows, float *scales, int32_t *meta) {
   int64_t row_bytes = orc_row_bytes(H, dtype);
+  int64_t in_row_bytes = orc_in_row_bytes(H, dtype);
   int64_t nsc = orc_scale_count(H, dtype);
   int64_t nslots = (int64_t)E * R * max_m;
-  for (int64_t i = 0; i < n_sel; ++i) {
+  uint8_t *qrow = (uint8_t *)malloc((size_t)(row_bytes > 0 ? row_bytes : 1));
+  float *qsc = (float *)malloc(sizeof(float) * (size_t)(nsc > 0 ? nsc : 1));
+  if (!qrow || !qsc) {
+    free(qrow);
+    free(qsc);
+    return ORC_EINVAL;
+  }
+  int st = ORC_OK;
+  for (int64_t i = 0; i < n_sel && st == ORC_OK; ++i) {
     int64_t tok = sel[i];
-    if (tok < 0 || tok >= (int64_t)R * T) return ORC_EINVAL;
+    if (tok < 0 || tok >= (int64_t)R * T) {
+      st = ORC_EINVAL;
+      break;
+    }
     int src = (int)(tok / T), t = (int)(tok % T);
+    /* the row and scales that go out: as given, or quantised once per token */
+    const uint8_t *row = x + tok * in_row_bytes;
+    const float *rsc = nsc > 0 && dtype == ORC_FP8_E4M3 ? x_scales + tok * nsc : qsc;
+    if (dtype == ORC_BF16_TO_FP8) {
+      orc_quantize_row((const uint16_t *)row, H, qrow, qsc);
+      row = qrow;
+    }
     for (int j = 0; j < k; ++j) {
       int64_t s = tok_slot[tok * k + j];
-      if (s < 0 || s >= nslots) return ORC_EINVAL;
+      if (s < 0 || s >= nslots) {
+        st = ORC_EINVAL;
+        break;
+      }
       int64_t region = s / max_m;
       int e = (int)(region / R);
-      if (region % R != src) return ORC_EINVAL; /* a slot belongs to its sender */
+      if (region % R != src) { /* a slot belongs to its sender */
+        st = ORC_EINVAL;
+        break;
+      }
       int64_t out = i * k + j;
       slot_id[out] = s;
-      memcpy(rows + out * row_bytes, x + tok * row_bytes, (size_t)row_bytes);
-      for (int64_t b = 0; b < nsc; ++b) scales[out * nsc + b] = x_scales[tok * nsc + b];
+      memcpy(rows + out * row_bytes, row, (size_t)row_bytes);
+      for (int64_t b = 0; b < nsc; ++b) scales[out * nsc + b] = rsc[b];
       meta[out * 4 + 0] = src;
       meta[out * 4 + 1] = t;
       meta[out * 4 + 2] = e;
       meta[out * 4 + 3] = j;
     }
   }
-  return ORC_OK;
+  free(qrow);
+  free(qsc);
+  return st;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -245,7 +322,7 @@ int orc_expert_stub(int R, int H, int E, int max_m, int dtype, int64_t n,
     if (e < 0 || e >= E) return ORC_EINVAL;
     const uint8_t *row = rows + i * row_bytes;
     uint16_t *yo = y + i * (int64_t)H;
-    if (dtype == ORC_FP8_E4M3) {
+    if (dtype != ORC_BF16) {
       double c = 1.0 + (double)e / 256.0;
       for (int h = 0; h < H; ++h) {
         double v = orc_e4m3_value(row[h]) * (double)scales[i * nsc + h / 128] * c;

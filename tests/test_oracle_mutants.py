@@ -24,13 +24,18 @@ MUTANTS = [
      "double w = (double)weights[tok * k + (k - 1 - j)];"),
     ("one expert dropped", "acc[h] = (j == 0) ? term : acc[h] + term;", "acc[h] = (j == 0) ? 0.0 : acc[h] + term;"),
     ("sum starts from +0", "acc[h] = (j == 0) ? term : acc[h] + term;", "acc[h] = (j == 0) ? 0.0 + term : acc[h] + term;"),
-    ("truncation instead of rounding", "double r = rint(a / quantum) * quantum;",
-     "double r = floor(a / quantum) * quantum;"),
+    ("truncation instead of rounding", "double r = rint(a / quantum) * quantum;\n  if (r >= 0x1p128)",
+     "double r = floor(a / quantum) * quantum;\n  if (r >= 0x1p128)"),
     ("bf16 subnormal spacing", "if (e < -126) e = -126;", "if (e < -140) e = -140;"),
     ("e4m3 exponent bias", "v = ldexp((double)(8 + m), ex - 10);", "v = ldexp((double)(8 + m), ex - 9);"),
     ("e4m3 subnormal scale", "v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
     ("header bytes dropped", "out[2] = slots * 16;", "out[2] = slots * 4;"),
     ("T > max_m accepted", "if (T > max_m) return ORC_EINVAL;", "if (T > 2 * max_m) return ORC_EINVAL;"),
+    ("e4m3 encoder truncates", "double r = rint(a / quantum) * quantum;\n  if (r < 0x1p-6)",
+     "double r = floor(a / quantum) * quantum;\n  if (r < 0x1p-6)"),
+    ("e4m3 subnormal boundary", "if (e < -6) e = -6;", "if (e < -7) e = -7;"),
+    ("e4m3 no saturation", "if (a >= 448.0) return (uint8_t)(sign | 0x7E);", "if (a >= 480.0) return (uint8_t)(sign | 0x7E);"),
+    ("quantiser scale off", "float s = amax > 0.0f ? amax / 448.0f : 1.0f;", "float s = amax > 0.0f ? amax / 447.0f : 1.0f;"),
 ]
 
 # the pins, cheapest first; each takes the (unused) oracle_lib fixture value
@@ -49,6 +54,9 @@ PINS = [
     lambda: pins.test_combine_identity_experts_return_the_input(None),
     lambda: pins.test_combine_scaling_experts_closed_form(None),
     lambda: pins.test_combine_is_linear_in_the_weights(None),
+    lambda: pins.test_e4m3_encoder_saturates_and_round_trips(None),
+    lambda: pins.test_e4m3_encoder_matches_torch(None),
+    lambda: pins.test_quantize_row_properties(None),
 ]
 
 

@@ -330,3 +330,75 @@ def test_combine_order_of_tokens_is_the_input_order(oracle_lib):
     sel = np.array([31, 0, 17, 5], np.int64)
     part = oracle.run(w, inp, sel)
     assert np.array_equal(part.out, full.out[sel])
+
+
+# --- quantise-on-dispatch (bf16 rows to E4M3 + 128-element scales) --------------
+
+def _e4m3_torch(vals32):
+    return torch.from_numpy(np.asarray(vals32, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_encoder_matches_torch(oracle_lib):
+    """Within the finite range, the nearest-even E4M3 code is torch's conversion."""
+    rng = np.random.default_rng(21)
+    finite = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    finite = finite[np.isfinite(finite)]
+    mags = np.unique(np.abs(finite))
+    ties = ((mags[:-1] + mags[1:]) / 2).astype(np.float32)           # exact midpoints
+    near = np.concatenate([ties * (1 + 2.0 ** -20), ties * (1 - 2.0 ** -20)]).astype(np.float32)
+    rand = (rng.standard_normal(20000) * 30).astype(np.float32)
+    tiny = (rng.random(2000) * 2.0 ** -6).astype(np.float32)           # the subnormal range
+    vals = np.concatenate([finite, ties, -ties, near, rand, tiny, -tiny])
+    vals = vals[np.abs(vals) <= 448]
+    got = np.array([oracle.e4m3_from_float(float(v)) for v in vals], np.uint8)
+    assert np.array_equal(got, _e4m3_torch(vals))
+
+
+def test_e4m3_encoder_saturates_and_round_trips(oracle_lib):
+    for v in (448.0, 449.0, 463.9, 464.0, 470.0, 479.0, 1e6, float("inf")):
+        assert oracle.e4m3_from_float(v) == 0x7E
+        assert oracle.e4m3_from_float(-v) == 0xFE
+    assert oracle.e4m3_from_float(2.0 ** -10) == 0x00     # halfway to the smallest subnormal: to even (0)
+    assert oracle.e4m3_from_float(3 * 2.0 ** -10) == 0x02  # halfway between m=1 and m=2: to even
+    for code in range(256):
+        v = oracle.e4m3_value(code)
+        if np.isfinite(v):
+            assert oracle.e4m3_from_float(v) == code
+
+
+def test_quantize_row_properties(oracle_lib):
+    rng = np.random.default_rng(8)
+    xf = rng.standard_normal(1024).astype(np.float32)
+    xf[256:384] = 0.0                                      # an all-zero block
+    bits = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    q, sc = oracle.quantize_row(bits)
+    xv = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    assert sc[2] == 1.0 and (q[256:384] == 0).all()
+    for b in range(8):
+        blk = slice(128 * b, 128 * (b + 1))
+        amax = np.abs(xv[blk]).max()
+        if amax == 0:
+            continue
+        assert sc[b] == np.float32(amax) / np.float32(448.0)
+        # the largest element maps to +-448 exactly
+        i = np.abs(xv[blk]).argmax() + 128 * b
+        assert (q[i] & 0x7F) == 0x7E
+        # each code is the torch conversion of x / scale taken in fp32
+        assert np.array_equal(q[blk], _e4m3_torch(xv[blk] / sc[b]))
+        deq = torch.from_numpy(q[blk]).view(torch.float8_e4m3fn).double().numpy() * sc[b]
+        assert (np.abs(deq - xv[blk]) <= 2 ** -4 * np.abs(xv[blk]) + sc[b] * 2 ** -9).all()
+
+
+def test_dispatch_quantises_each_token_once(oracle_lib):
+    w = wl.WORKLOADS["ds_decode_bf16in"]
+    w = wl.custom("q_small", num_ranks=2, tokens_per_rank=6, hidden=256, num_experts=8, topk=3, max_m=6,
+                  dtype="bf16q", expert="scale", x_dist="normal")
+    inp = wl.make_inputs(w)
+    assert inp.x.dtype == np.uint16 and inp.x_scales is None
+    _, _, tok_slot = oracle.layout(inp.topk_idx, 8, 6)
+    sl = oracle.dispatch(inp.x, None, tok_slot, 8, 6, oracle.BF16_TO_FP8)
+    assert sl.rows.shape == (12 * 3, 256) and sl.scales.shape == (12 * 3, 2)
+    for i in range(12):
+        q, sc = oracle.quantize_row(inp.x.reshape(12, 256)[i])
+        for j in range(3):
+            assert np.array_equal(sl.rows[i * 3 + j], q) and np.array_equal(sl.scales[i * 3 + j], sc)
