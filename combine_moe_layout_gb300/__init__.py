@@ -7,6 +7,7 @@ seeded workload generators.
 """
 from ._binding import (  # noqa: F401
     MOE_BF16,
+    MOE_BF16_TO_FP8,
     MOE_EINVAL,
     MOE_ECUDA,
     MOE_ENOMEM,

@@ -15,7 +15,7 @@ import torch
 from . import _build
 
 MOE_OK, MOE_EINVAL, MOE_EOVERFLOW, MOE_ETIMEOUT, MOE_ECUDA, MOE_ENOMEM = 0, -1, -2, -3, -4, -5
-MOE_BF16, MOE_FP8_E4M3 = 0, 1
+MOE_BF16, MOE_FP8_E4M3, MOE_BF16_TO_FP8 = 0, 1, 2
 
 
 class MoeDesc(ctypes.Structure):
@@ -178,7 +178,7 @@ def allocate_buffers(desc: MoeDesc, device, with_expert_out: bool | None = None)
     sz = moe_buffer_sizes(desc)
     R, T, H, E, k, M = desc.num_ranks, desc.tokens_per_rank, desc.hidden, desc.num_experts, desc.topk, desc.max_m
     slots = E * R * M
-    fp8 = desc.dtype == MOE_FP8_E4M3
+    fp8 = desc.dtype != MOE_BF16  # slots hold e4m3 rows + scales
     dev = torch.device(device)
     recv_x = torch.empty(sz["recv_x"], dtype=torch.uint8, device=dev).view(slots, -1)
     recv_scales = torch.empty((slots, H // 128), dtype=torch.float32, device=dev) if fp8 else None

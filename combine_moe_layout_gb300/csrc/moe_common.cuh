@@ -74,6 +74,12 @@ __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Order this thread's generic-proxy shared memory accesses before later
+// async-proxy (TMA) accesses to the same shared memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                "r"(bytes)
@@ -136,14 +142,46 @@ __device__ __forceinline__ void grid_dependents_launch() {
 }
 
 // ---------------------------------------------------------------------------
+// Quantise-on-dispatch: bf16 blocks of 128 elements -> E4M3 + one fp32 scale.
+// scale = amax / 448 (1 for an all-zero block); code = e4m3(x / scale), with
+// IEEE fp32 division and the hardware's round-to-nearest-even, saturating
+// conversion. Warp w of nwarps handles blocks w, w + nwarps, ...; each lane
+// takes 4 consecutive elements. src, dst and sc are shared memory.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint16_t e4m3x2_rn_satfinite(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;  // lo in the low byte, hi in the high byte
+}
+
+__device__ __forceinline__ void quantize_blocks(const uint16_t *src, uint8_t *dst, float *sc, int nblk, int warp,
+                                                int nwarps, int lane) {
+  for (int b = warp; b < nblk; b += nwarps) {
+    const uint2 raw = *reinterpret_cast<const uint2 *>(src + b * kScaleBlock + lane * 4);
+    const float f0 = __uint_as_float(raw.x << 16), f1 = __uint_as_float(raw.x & 0xffff0000u);
+    const float f2 = __uint_as_float(raw.y << 16), f3 = __uint_as_float(raw.y & 0xffff0000u);
+    float amax = fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    const uint32_t q = static_cast<uint32_t>(e4m3x2_rn_satfinite(__fdiv_rn(f0, s), __fdiv_rn(f1, s))) |
+                       (static_cast<uint32_t>(e4m3x2_rn_satfinite(__fdiv_rn(f2, s), __fdiv_rn(f3, s))) << 16);
+    *reinterpret_cast<uint32_t *>(dst + b * kScaleBlock + lane * 4) = q;
+    if (lane == 0) sc[b] = s;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
 struct Sizes {
   int R, T, H, E, k, max_m, dtype, L;
   int64_t nslots;     // E * R * max_m
   int64_t ntok;       // R * T
-  int64_t row_bytes;  // 2H (bf16) or H (fp8)
-  int nsc;            // scales per row (H/128 for fp8, 0 for bf16)
+  int64_t row_bytes;     // bytes of a dispatched row: 2H (bf16) or H (fp8, bf16-to-fp8)
+  int64_t in_row_bytes;  // bytes of a caller's input row: H (fp8) or 2H (bf16, bf16-to-fp8)
+  int nsc;               // scales per dispatched row (H/128, 0 for bf16)
+  bool quant;            // bf16 input rows quantised to fp8 on dispatch
 };
 
 // Independent restatement of the desc rules (see moe_layout.h).
@@ -153,7 +191,7 @@ inline moe_status check_desc(const moe_desc *d, Sizes *s) {
             M = d->max_m;
   if (R < 1 || T < 0 || H < 1 || E < 1 || k < 1 || M < 1) return MOE_EINVAL;
   if (E % R != 0 || k > E || k > kMaxTopk || T > M) return MOE_EINVAL;
-  if (d->dtype == MOE_FP8_E4M3) {
+  if (d->dtype == MOE_FP8_E4M3 || d->dtype == MOE_BF16_TO_FP8) {
     if (H % kScaleBlock != 0) return MOE_EINVAL;
   } else if (d->dtype == MOE_BF16) {
     if (H % 8 != 0) return MOE_EINVAL;
@@ -174,8 +212,10 @@ inline moe_status check_desc(const moe_desc *d, Sizes *s) {
     s->L = E / R;
     s->nslots = static_cast<int64_t>(E) * R * M;
     s->ntok = static_cast<int64_t>(R) * T;
-    s->row_bytes = d->dtype == MOE_FP8_E4M3 ? H : 2 * static_cast<int64_t>(H);
-    s->nsc = d->dtype == MOE_FP8_E4M3 ? H / kScaleBlock : 0;
+    s->row_bytes = d->dtype == MOE_BF16 ? 2 * static_cast<int64_t>(H) : H;
+    s->in_row_bytes = d->dtype == MOE_FP8_E4M3 ? H : 2 * static_cast<int64_t>(H);
+    s->nsc = d->dtype == MOE_BF16 ? 0 : H / kScaleBlock;
+    s->quant = d->dtype == MOE_BF16_TO_FP8;
   }
   return MOE_OK;
 }

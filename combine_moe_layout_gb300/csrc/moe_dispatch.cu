@@ -35,7 +35,10 @@ struct DispatchArgs {
   float *recv_scales;
   int4 *recv_meta;
   int32_t *err;
-  int R, T, k, max_m, nsc, stages, pieces, early;
+  int R, T, k, max_m, nsc, stages, pieces, early, quant;
+  // row_bytes, piece_bytes: of the caller's input rows. Copy mode dispatches
+  // them as they are; quant mode turns each 256-byte bf16 block of a piece into
+  // 128 e4m3 bytes (the dispatched row has row_bytes / 2 bytes) and one scale.
   uint32_t row_bytes, piece_bytes;
   int64_t nslots, nunits;
 };
@@ -46,6 +49,17 @@ __device__ __forceinline__ void issue_unit_load(const DispatchArgs &a, uint8_t *
   const uint32_t bytes = min(a.piece_bytes, a.row_bytes - off);
   mbar_arrive_expect_tx(bar, bytes);
   bulk_load(stage, a.x + row * a.row_bytes + off, bytes, bar);
+}
+
+// Quant mode: shared memory holds S input stages, then S e4m3 stages of half
+// their size, then S scale buffers of piece_bytes / 256 floats.
+__device__ __forceinline__ uint8_t *qstage(const DispatchArgs &a, uint8_t *base, int s) {
+  return base + static_cast<size_t>(a.stages) * a.piece_bytes + static_cast<size_t>(s) * (a.piece_bytes / 2);
+}
+__device__ __forceinline__ float *qscales(const DispatchArgs &a, uint8_t *base, int s) {
+  return reinterpret_cast<float *>(base + static_cast<size_t>(a.stages) * a.piece_bytes +
+                                   static_cast<size_t>(a.stages) * (a.piece_bytes / 2)) +
+         static_cast<size_t>(s) * (a.piece_bytes / 256);
 }
 
 __global__ void __launch_bounds__(32) dispatch_kernel(DispatchArgs a) {
@@ -106,7 +120,7 @@ __global__ void __launch_bounds__(32) dispatch_kernel(DispatchArgs a) {
         const int32_t slot = dst[lane];
         a.recv_meta[slot] = make_int4(src, t, (slot / a.max_m) / a.R, lane);
       }
-      if (a.nsc > 0) {
+      if (a.nsc > 0 && !a.quant) {
         const float *sc = a.x_scales + row * a.nsc;
         for (int q = lane; q < a.k * a.nsc; q += 32) {
           const int j = q / a.nsc, c = q - j * a.nsc;
@@ -114,6 +128,44 @@ __global__ void __launch_bounds__(32) dispatch_kernel(DispatchArgs a) {
           if (slot >= 0) a.recv_scales[static_cast<int64_t>(slot) * a.nsc + c] = __ldg(sc + c);
         }
       }
+    }
+
+    if (a.quant) {
+      // every lane reads the staged bf16 piece: wait for it
+      uint8_t *stage = dsm + static_cast<size_t>(s) * a.piece_bytes;
+      if (!mbar_wait_bounded(&full[s], parity)) {
+        latch_error(a.err, MOE_ETIMEOUT);
+        aborted = 1;
+      }
+      __syncwarp();
+      if (aborted) break;
+      // the e4m3 stage of unit i - S may still be read by its bulk stores
+      if (lane == 0 && i >= S) bulk_wait_read<0>();
+      __syncwarp();
+      uint8_t *q = qstage(a, dsm, s);
+      float *qs = qscales(a, dsm, s);
+      const int nblk = static_cast<int>(bytes / 256);
+      quantize_blocks(reinterpret_cast<const uint16_t *>(stage), q, qs, nblk, 0, 1, lane);
+      fence_proxy_async_smem();  // the shared writes above, before the bulk stores and the refill
+      __syncwarp();
+      const int sc0 = static_cast<int>(off / 256);
+      for (int qq = lane; qq < a.k * nblk; qq += 32) {
+        const int j = qq / nblk, b = qq - j * nblk;
+        const int32_t slot = dst[j];
+        if (slot >= 0) a.recv_scales[static_cast<int64_t>(slot) * a.nsc + sc0 + b] = qs[b];
+      }
+      if (lane == 0) {
+        for (int j = 0; j < a.k; ++j) {
+          const int32_t slot = dst[j];
+          if (slot >= 0)
+            bulk_store(a.recv_x + static_cast<int64_t>(slot) * (a.row_bytes / 2) + off / 2, q, bytes / 2);
+        }
+        bulk_commit();
+        // the bf16 stage has been consumed: refill it with unit i + S
+        if (i + S < n_mine) issue_unit_load(a, stage, &full[s], first + (i + S) * stride);
+      }
+      __syncwarp();
+      continue;
     }
 
     if (lane == 0) {
@@ -143,7 +195,7 @@ __global__ void __launch_bounds__(32) dispatch_kernel(DispatchArgs a) {
   if (lane == 0) {
     if (aborted) {
       // drain the loads still in flight (bounded) before the CTA releases its shared memory
-      const int64_t issued = inflight_end(i, S, n_mine);
+      const int64_t issued = a.quant ? (n_mine < i + S ? n_mine : i + S) : inflight_end(i, S, n_mine);
       for (int64_t u = i; u < issued; ++u)
         mbar_wait_bounded(&full[u % S], static_cast<uint32_t>((u / S) & 1));
     }
@@ -170,8 +222,9 @@ moe_status launch_dispatch(const Sizes &s, const void *x, const float *x_scales,
   a.max_m = s.max_m;
   a.nsc = s.nsc;
   a.early = early_trigger(s.ntok);
-  a.row_bytes = static_cast<uint32_t>(s.row_bytes);
-  a.piece_bytes = a.row_bytes < kPieceMax ? a.row_bytes : kPieceMax;
+  a.quant = s.quant ? 1 : 0;
+  a.row_bytes = static_cast<uint32_t>(s.in_row_bytes);
+  a.piece_bytes = a.row_bytes < kPieceMax ? a.row_bytes : kPieceMax;  // a multiple of 256 in quant mode
   a.pieces = static_cast<int>((a.row_bytes + a.piece_bytes - 1) / a.piece_bytes);
   a.nslots = s.nslots;
   a.nunits = s.ntok * a.pieces;
@@ -179,7 +232,12 @@ moe_status launch_dispatch(const Sizes &s, const void *x, const float *x_scales,
   a.stages = stages < 2 ? 2 : (stages > kMaxStages ? kMaxStages : stages);
   if (a.nunits == 0) return MOE_OK;
 
-  const size_t smem = static_cast<size_t>(a.stages) * a.piece_bytes;
+  size_t smem = static_cast<size_t>(a.stages) * a.piece_bytes;
+  if (a.quant) smem += static_cast<size_t>(a.stages) * (a.piece_bytes / 2 + a.piece_bytes / 256 * sizeof(float));
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+          cudaSuccess)
+    return MOE_ECUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel, 32, smem) != cudaSuccess)
     return MOE_ECUDA;
@@ -214,6 +272,8 @@ extern "C" moe_status moe_dispatch(const moe_desc *desc, const void *x, const fl
   if (s.dtype == MOE_FP8_E4M3) {
     if (recv_scales == nullptr || (s.ntok > 0 && x_scales == nullptr)) return MOE_EINVAL;
     if (!aligned4(x_scales) || !aligned4(recv_scales)) return MOE_EINVAL;
+  } else if (s.dtype == MOE_BF16_TO_FP8) {
+    if (recv_scales == nullptr || x_scales != nullptr || !aligned4(recv_scales)) return MOE_EINVAL;
   }
   if (!aligned16(x) || !aligned16(recv_x) || !aligned16(recv_meta) || !aligned4(tok_slot) || !aligned4(err))
     return MOE_EINVAL;

@@ -99,7 +99,7 @@ extern "C" moe_status moe_expert_stub(const moe_desc *desc, const void *recv_x, 
   Sizes s;
   moe_status st = check_desc(desc, &s);
   if (st != MOE_OK) return st;
-  if (s.dtype != MOE_FP8_E4M3) return MOE_EINVAL;
+  if (s.dtype == MOE_BF16) return MOE_EINVAL;
   if (recv_x == nullptr || recv_scales == nullptr || counts == nullptr || expert_out == nullptr || err == nullptr)
     return MOE_EINVAL;
   if (!aligned16(recv_x) || !aligned16(expert_out) || !aligned4(recv_scales) || !aligned4(counts))

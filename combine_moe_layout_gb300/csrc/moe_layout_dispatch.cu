@@ -38,8 +38,10 @@ struct FusedArgs {
   float *recv_scales;
   int4 *recv_meta;
   int32_t *err;
-  int R, T, E, k, max_m, nsc, words, ctas_per_rank, stages, early;
-  uint32_t row_bytes;
+  int R, T, E, k, max_m, nsc, words, ctas_per_rank, stages, early, quant;
+  uint32_t row_bytes;     // a dispatched row (the slot stride)
+  uint32_t in_row_bytes;  // a caller's input row (the stage size)
+  uint32_t qoff;          // quant mode: offset of the e4m3 row buffer in shared memory
   int64_t nslots;
 };
 
@@ -55,8 +57,10 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
   const int S = a.stages;
   // rows t = c, c + C, c + 2C, ... of source rank src
   const int n_mine = c < a.T ? (a.T - 1 - c) / a.ctas_per_rank + 1 : 0;
-  uint32_t *bits = reinterpret_cast<uint32_t *>(fsm + static_cast<size_t>(S) * a.row_bytes);
-  const uint8_t *xs = a.x + static_cast<int64_t>(src) * a.T * a.row_bytes;
+  uint32_t *bits = reinterpret_cast<uint32_t *>(fsm + static_cast<size_t>(S) * a.in_row_bytes);
+  const uint8_t *xs = a.x + static_cast<int64_t>(src) * a.T * a.in_row_bytes;
+  uint8_t *qbuf = fsm + a.qoff;                                   // quant mode: e4m3 row
+  float *qsc = reinterpret_cast<float *>(fsm + a.qoff + a.row_bytes);  // quant mode: its scales
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
@@ -64,9 +68,9 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
     aborted = 0;
     for (int i = 0; i < n_mine && i < S; ++i) {
       const int t = c + i * a.ctas_per_rank;
-      mbar_arrive_expect_tx(&full[i], a.row_bytes);
-      bulk_load(fsm + static_cast<size_t>(i) * a.row_bytes, xs + static_cast<int64_t>(t) * a.row_bytes,
-                a.row_bytes, &full[i]);
+      mbar_arrive_expect_tx(&full[i], a.in_row_bytes);
+      bulk_load(fsm + static_cast<size_t>(i) * a.in_row_bytes, xs + static_cast<int64_t>(t) * a.in_row_bytes,
+                a.in_row_bytes, &full[i]);
     }
   }
   grid_dependency_wait();
@@ -122,6 +126,37 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
       if (slot >= 0) a.recv_meta[slot] = make_int4(src, t, e, tid);
     }
     __syncthreads();
+    if (a.quant) {
+      uint8_t *stage = fsm + static_cast<size_t>(s) * a.in_row_bytes;
+      if (!mbar_wait_bounded(&full[s], parity)) {  // every thread reads the staged bf16 row
+        latch_error(a.err, MOE_ETIMEOUT);
+        aborted = 1;
+      }
+      if (tid == 0 && i > 0) bulk_wait_read<0>();  // the previous row's stores may still read qbuf
+      __syncthreads();
+      if (aborted) break;
+      quantize_blocks(reinterpret_cast<const uint16_t *>(stage), qbuf, qsc, a.nsc, tid >> 5, kFusedThreads / 32,
+                      tid & 31);
+      fence_proxy_async_smem();  // the shared writes above, before the bulk stores and the refill
+      __syncthreads();
+      for (int q = tid; q < a.k * a.nsc; q += kFusedThreads) {
+        const int j = q / a.nsc, cc = q - j * a.nsc;
+        const int32_t slot = dst[j];
+        if (slot >= 0) a.recv_scales[static_cast<int64_t>(slot) * a.nsc + cc] = qsc[cc];
+      }
+      if (tid == 0) {
+        for (int j = 0; j < a.k; ++j)
+          if (dst[j] >= 0) bulk_store(a.recv_x + static_cast<int64_t>(dst[j]) * a.row_bytes, qbuf, a.row_bytes);
+        bulk_commit();
+        if (i + S < n_mine) {  // the bf16 stage has been consumed: refill it with row i + S
+          const int tn = c + (i + S) * a.ctas_per_rank;
+          mbar_arrive_expect_tx(&full[s], a.in_row_bytes);
+          bulk_load(stage, xs + static_cast<int64_t>(tn) * a.in_row_bytes, a.in_row_bytes, &full[s]);
+        }
+      }
+      __syncthreads();
+      continue;
+    }
     if (a.nsc > 0) {
       const float *sc = a.x_scales + row * a.nsc;
       for (int q = tid; q < a.k * a.nsc; q += kFusedThreads) {
@@ -131,7 +166,7 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
       }
     }
     if (tid == 0) {
-      uint8_t *stage = fsm + static_cast<size_t>(s) * a.row_bytes;
+      uint8_t *stage = fsm + static_cast<size_t>(s) * a.in_row_bytes;
       if (!mbar_wait_bounded(&full[s], parity)) {
         latch_error(a.err, MOE_ETIMEOUT);
         aborted = 1;
@@ -144,9 +179,9 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
           bulk_wait_read<1>();
           const int ps = (i - 1) % S;
           const int tn = c + next * a.ctas_per_rank;
-          mbar_arrive_expect_tx(&full[ps], a.row_bytes);
-          bulk_load(fsm + static_cast<size_t>(ps) * a.row_bytes, xs + static_cast<int64_t>(tn) * a.row_bytes,
-                    a.row_bytes, &full[ps]);
+          mbar_arrive_expect_tx(&full[ps], a.in_row_bytes);
+          bulk_load(fsm + static_cast<size_t>(ps) * a.in_row_bytes, xs + static_cast<int64_t>(tn) * a.in_row_bytes,
+                    a.in_row_bytes, &full[ps]);
         }
       }
     }
@@ -156,18 +191,26 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
   if (tid == 0) {
     if (aborted) {
       // drain the loads still in flight (bounded) before the CTA releases its shared memory
-      const int issued = static_cast<int>(inflight_end(i, S, n_mine));
+      const int issued = a.quant ? min(n_mine, i + S) : static_cast<int>(inflight_end(i, S, n_mine));
       for (int u = i; u < issued; ++u) mbar_wait_bounded(&full[u % S], static_cast<uint32_t>((u / S) & 1));
     }
     bulk_wait_all();
   }
 }
 
+// Offset of the e4m3 row buffer (quant mode): after the row stages and the bitmaps.
+static size_t fused_qoff(const Sizes &s, int stages) {
+  const int words = (s.T + 31) / 32;
+  const size_t end = static_cast<size_t>(stages) * s.in_row_bytes + static_cast<size_t>(s.E) * (words > 0 ? words : 1) * 4;
+  return (end + 127) / 128 * 128;
+}
+
 // Whether one CTA can hold a source rank's bitmaps next to its row stages.
 static bool fused_fits(const Sizes &s, int stages, size_t *smem) {
-  if (s.T > kFusedMaxTokens || s.row_bytes > kFusedMaxRowBytes || s.row_bytes % 16 != 0) return false;
+  if (s.T > kFusedMaxTokens || s.in_row_bytes > kFusedMaxRowBytes || s.in_row_bytes % 16 != 0) return false;
   const int words = (s.T + 31) / 32;
-  *smem = static_cast<size_t>(stages) * s.row_bytes + static_cast<size_t>(s.E) * (words > 0 ? words : 1) * 4;
+  *smem = static_cast<size_t>(stages) * s.in_row_bytes + static_cast<size_t>(s.E) * (words > 0 ? words : 1) * 4;
+  if (s.quant) *smem = fused_qoff(s, stages) + static_cast<size_t>(s.row_bytes) + static_cast<size_t>(s.nsc) * 4;
   return *smem <= kFusedMaxSmem;
 }
 
@@ -205,13 +248,16 @@ moe_status launch_layout_dispatch(const Sizes &s, const int32_t *topk_idx, const
   a.nsc = s.nsc;
   a.words = (s.T + 31) / 32;
   a.early = early_trigger(s.ntok);
+  a.quant = s.quant ? 1 : 0;
   a.row_bytes = static_cast<uint32_t>(s.row_bytes);
+  a.in_row_bytes = static_cast<uint32_t>(s.in_row_bytes);
   a.nslots = s.nslots;
 
   const int sms = num_sms > 0 && num_sms < sm_count() ? num_sms : sm_count();
   // first try one row per CTA (one stage); with fewer CTAs than rows use two stages
   for (int stages = 1; stages <= 2; ++stages) {
     if (!fused_fits(s, stages, &smem)) return MOE_EINVAL;
+    a.qoff = static_cast<uint32_t>(fused_qoff(s, stages));
     if (smem > 48 * 1024 && cudaFuncSetAttribute(layout_dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem)) != cudaSuccess)
       return MOE_ECUDA;
@@ -258,6 +304,8 @@ extern "C" moe_status moe_layout_dispatch(const moe_desc *desc, const int32_t *t
   if (s.dtype == MOE_FP8_E4M3) {
     if (recv_scales == nullptr || (s.ntok > 0 && x_scales == nullptr)) return MOE_EINVAL;
     if (!aligned4(x_scales) || !aligned4(recv_scales)) return MOE_EINVAL;
+  } else if (s.dtype == MOE_BF16_TO_FP8) {
+    if (recv_scales == nullptr || x_scales != nullptr || !aligned4(recv_scales)) return MOE_EINVAL;
   }
   if (!aligned16(x) || !aligned16(recv_x) || !aligned16(recv_meta) || !aligned4(tok_slot) || !aligned4(err) ||
       !aligned4(topk_idx) || !aligned4(counts) || (reinterpret_cast<uintptr_t>(flags) & 7u) != 0)

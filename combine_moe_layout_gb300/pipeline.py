@@ -57,7 +57,7 @@ class MoeStep:
     def __init__(self, workload, device="cuda", num_sms: int = 0, buffers: B.MoeBuffers | None = None):
         self.w = workload
         self.desc = B.MoeDesc.of(workload, num_sms)
-        self.fp8 = workload.dtype == "fp8"
+        self.fp8 = workload.dtype != "bf16"  # slots hold e4m3 rows + scales
         self.device = torch.device(device)
         self.buf = buffers if buffers is not None else B.allocate_buffers(self.desc, self.device)
         self.slots = workload.num_experts * workload.num_ranks * workload.max_m

@@ -70,15 +70,20 @@ typedef enum {
 } moe_status;
 
 typedef enum {
-  MOE_BF16 = 0,     /* rows of H bfloat16 */
-  MOE_FP8_E4M3 = 1  /* rows of H e4m3 bytes + H/128 fp32 scales */
+  MOE_BF16 = 0,       /* rows of H bfloat16 */
+  MOE_FP8_E4M3 = 1,   /* rows of H e4m3 bytes + H/128 fp32 scales */
+  MOE_BF16_TO_FP8 = 2 /* the caller's rows are H bfloat16; dispatch quantises each row once to H e4m3
+                         bytes + H/128 fp32 scales (scale = amax/448 of 128 contiguous elements, code =
+                         nearest-even e4m3 of x/scale in fp32, saturated to +-448) and the slots hold
+                         those ("NVSHMEM and DeepEP", high-throughput section: FP8 dispatch with
+                         fine-grained scales) */
 } moe_dtype;
 
 /* The problem statement: tokens, routing, EP ranks and the per-rank bound. */
 typedef struct {
   int32_t num_ranks;       /* R >= 1 */
   int32_t tokens_per_rank; /* 0 <= T <= max_m */
-  int32_t hidden;          /* H; multiple of 8 (bf16) or of 128 (fp8) */
+  int32_t hidden;          /* H; multiple of 8 (bf16) or of 128 (fp8, bf16-to-fp8) */
   int32_t num_experts;     /* E, a multiple of R */
   int32_t topk;            /* 1 <= k <= min(E, 16) */
   int32_t max_m;           /* slots per (expert, source rank), >= 1 */
@@ -123,11 +128,13 @@ moe_status moe_layout(const moe_desc *desc, const int32_t *topk_idx, int32_t *co
  * low-latency section). Waits, bounded, until the count+1 flag of each
  * destination region is non-zero, then copies row (src, t) and its scales into
  * each of its k slots and writes the slot header {src, t, e, j}.
- *   x [R][T] rows: H bf16 (2H bytes) or H e4m3 bytes; 16-byte aligned (read).
- *   x_scales [R][T][H/128] float (fp8 only; NULL for bf16) (read).
+ *   x [R][T] rows: H bf16 (2H bytes; also for MOE_BF16_TO_FP8) or H e4m3 bytes;
+ *   16-byte aligned (read).
+ *   x_scales [R][T][H/128] float (MOE_FP8_E4M3 only; NULL otherwise) (read).
  *   tok_slot, flags: from moe_layout (read).
- *   recv_x [E][R][max_m] rows, 16-byte aligned; recv_scales [E][R][max_m][H/128]
- *   (fp8 only; NULL for bf16); recv_meta [E][R][max_m][4] int32, 16-byte
+ *   recv_x [E][R][max_m] dispatched rows (2H bytes bf16, H bytes otherwise),
+ *   16-byte aligned; recv_scales [E][R][max_m][H/128] (NULL for bf16);
+ *   recv_meta [E][R][max_m][4] int32, 16-byte
  *   aligned (written; only slots pos < count are touched).
  * Device errors: a flag still zero after the bounded wait -> MOE_ETIMEOUT;
  * tok_slot out of range -> MOE_EINVAL; the affected copies are skipped. */
@@ -152,7 +159,7 @@ moe_status moe_layout_dispatch(const moe_desc *desc, const int32_t *topk_idx, co
 int32_t moe_layout_dispatch_kernels(const moe_desc *desc);
 
 /* Synthetic experts for tests and benchmarks (not part of the pages' method):
- * for every filled slot (pos < counts) of an fp8 step,
+ * for every filled slot (pos < counts) of an fp8 or bf16-to-fp8 step,
  * expert_out = bf16_rne(e4m3(q) * scale * (1 + e/256)), the product taken
  * exactly and rounded once. bf16 steps use identity experts: pass recv_x as
  * expert_out to moe_combine instead (this call returns MOE_EINVAL for bf16).

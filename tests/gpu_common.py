@@ -50,7 +50,7 @@ def guarded_buffers(desc, device):
     """MoeBuffers whose every tensor sits between guard bands."""
     R, T, H, E, k, M = desc.num_ranks, desc.tokens_per_rank, desc.hidden, desc.num_experts, desc.topk, desc.max_m
     slots = E * R * M
-    fp8 = desc.dtype == B.MOE_FP8_E4M3
+    fp8 = desc.dtype != B.MOE_BF16  # slots hold e4m3 rows + scales
     row = H if fp8 else 2 * H
     g = {
         "counts": Guarded((E, R), torch.int32, device, 0),

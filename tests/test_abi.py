@@ -44,6 +44,7 @@ def test_library_is_built_for_sm_103a():
 @pytest.mark.parametrize("shape", [
     (2, 16, 128, 8, 2, 16, 0), (8, 128, 7168, 256, 8, 128, 1), (8, 4096, 4096, 8, 2, 4096, 0),
     (16, 256, 7168, 256, 8, 256, 0), (8, 4096, 7168, 256, 8, 4096, 1), (64, 128, 7168, 256, 8, 128, 1),
+    (8, 128, 7168, 256, 8, 128, 2),
 ])
 def test_buffer_sizes_agree_with_the_oracle(shape):
     R, T, H, E, k, M, dt = shape
@@ -59,7 +60,8 @@ def test_buffer_sizes_agree_with_the_oracle(shape):
     (2, 16, 192, 8, 2, 16, 1),    # fp8 hidden not whole 128-element blocks
     (2, 16, 128, 8, 9, 16, 0),    # k > E
     (2, 16, 128, 64, 17, 16, 0),  # k > 16
-    (2, 16, 128, 8, 2, 16, 2),    # unknown dtype
+    (2, 16, 128, 8, 2, 16, 3),    # unknown dtype
+    (2, 16, 192, 8, 2, 16, 2),    # bf16 rows quantised on dispatch need whole 128-element blocks
     (0, 16, 128, 8, 2, 16, 0),    # no ranks
 ])
 def test_invalid_descs_are_rejected_on_the_host(shape):

@@ -170,6 +170,11 @@ EDGE = {
                                 max_m=4096, x_dist="normal"),
     "tma_combine_k4_fp8": dict(num_ranks=8, tokens_per_rank=2048, hidden=1024, num_experts=32, topk=4,
                                max_m=2048, dtype="fp8", expert="scale", x_dist="normal", renormalize=False),
+    # bf16 rows quantised to fp8 on dispatch: rows of two 16 KiB pieces, and one scale per row with k = 16
+    "quant_two_pieces": dict(num_ranks=2, tokens_per_rank=40, hidden=16384, num_experts=8, topk=2, max_m=40,
+                             dtype="bf16q", expert="scale", x_dist="normal"),
+    "quant_k16_one_scale": dict(num_ranks=2, tokens_per_rank=130, hidden=128, num_experts=32, topk=16, max_m=200,
+                                dtype="bf16q", expert="scale", x_dist="normal"),
     # 4096 experts: the cluster's bitmaps do not fit, the chunked layout kernel runs
     "many_experts_chunked": dict(num_ranks=1, tokens_per_rank=1024, hidden=64, num_experts=4096, topk=2,
                                  max_m=1024),
@@ -351,3 +356,36 @@ def test_pinned_host_inputs_and_output(name, fused):
     torch.cuda.synchronize()
     assert torch.equal(hout.view(torch.int16), ref.cpu().view(torch.int16))
     assert torch.equal(step.buf.recv_meta, ref_meta)
+
+
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+def test_ds_decode_bf16_rows_quantised_on_dispatch(fused):
+    """bf16 input rows: the slots hold the oracle's E4M3 codes and scales bit for bit."""
+    w = wl.WORKLOADS["ds_decode_bf16in"]
+    if fused:
+        assert B.moe_layout_dispatch_kernels(B.MoeDesc.of(w)) == 1
+    inp = wl.make_inputs(w)
+    step, d, ref, out = _full_parity(w, inp, region_sets=False, fused=fused)
+    # the dispatched rows are half the input bytes
+    assert step.buf.recv_x.shape[1] == w.hidden
+
+
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+@pytest.mark.parametrize("num_sms", [1, 4])
+def test_quantised_dispatch_deep_pipeline(num_sms, fused):
+    w = wl.custom("qdeep", num_ranks=4, tokens_per_rank=300, hidden=1024, num_experts=16, topk=4, max_m=300,
+                  dtype="bf16q", expert="scale", x_dist="normal", renormalize=False)
+    _full_parity(w, wl.make_inputs(w, seed=12), num_sms=num_sms, region_sets=False, fused=fused)
+
+
+def test_quantised_dispatch_rejects_input_scales():
+    w = wl.custom("qrej", num_ranks=2, tokens_per_rank=8, hidden=256, num_experts=4, topk=2, max_m=8,
+                  dtype="bf16q", expert="scale", x_dist="normal")
+    step = P.MoeStep(w, "cuda:0")
+    d = P.to_device(wl.make_inputs(w), "cuda:0")
+    bogus = torch.ones((2, 8, 2), dtype=torch.float32, device="cuda:0")
+    step.reset()
+    step.layout(d)
+    with pytest.raises(B.MoeError):
+        B.moe_dispatch(step.desc, d.x, bogus, step.buf.tok_slot, step.buf.flags, step.buf.recv_x,
+                       step.buf.recv_scales, step.buf.recv_meta, step.buf.err)
