@@ -84,6 +84,10 @@ def _bind(path: str):
     lib.orc_e4m3_from_float.restype = ctypes.c_uint8
     lib.orc_quantize_row.argtypes = [vp, i32, vp, vp]
     lib.orc_quantize_row.restype = None
+    lib.orc_region_offsets.argtypes = [i32, i32, i32, vp, vp]
+    lib.orc_region_offsets.restype = i32
+    lib.orc_compact.argtypes = [i32, i32, i32, i64, i32, vp, i64, vp, vp, vp, vp, i64, vp, vp, vp]
+    lib.orc_compact.restype = i32
     lib.orc_validate.argtypes = [i32] * 7
     lib.orc_validate.restype = i32
     lib.orc_buffer_sizes.argtypes = [i32] * 7 + [vp]
@@ -255,6 +259,36 @@ def combine(tok_slot: np.ndarray, topk_weights: np.ndarray, slot_id: np.ndarray,
     yy = np.ascontiguousarray(y, dtype=np.uint16)
     _check(_load().orc_combine(R, T, H, num_experts, k, max_m, sel.size, _p(sel), _p(ts), _p(w), sid.size,
                                _p(sid), _p(yy), _p(out)), "combine")
+    return out
+
+
+def region_offsets(counts: np.ndarray, max_m: int) -> np.ndarray:
+    """Exclusive prefix of the counts in (expert, source rank) order, plus the total: int32 [E*R + 1]."""
+    c = np.ascontiguousarray(counts, dtype=np.int32)
+    E, R = c.shape
+    out = np.zeros(E * R + 1, np.int32)
+    _check(_load().orc_region_offsets(R, E, max_m, _p(c), _p(out)), "region_offsets")
+    return out
+
+
+@dataclass
+class Packed:
+    rows: np.ndarray     # [n, row_bytes] uint8
+    scales: np.ndarray   # [n, H/128] float32
+    meta: np.ndarray     # [n, 4] int32
+
+
+def compact(slots: SparseSlots, offsets: np.ndarray, R: int, E: int, max_m: int, n_packed: int) -> Packed:
+    """Packed (expert, source rank, position) rows of the given sparse slots."""
+    n = slots.slot_id.size
+    rb = slots.rows.shape[1]
+    nsc = slots.scales.shape[1]
+    out = Packed(np.zeros((n_packed, rb), np.uint8), np.zeros((n_packed, nsc), np.float32),
+                 np.zeros((n_packed, 4), np.int32))
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    _check(_load().orc_compact(R, E, max_m, rb, nsc, _p(off), n, _p(slots.slot_id), _p(slots.rows),
+                               _p(slots.scales), _p(slots.meta), n_packed, _p(out.rows), _p(out.scales),
+                               _p(out.meta)), "compact")
     return out
 
 

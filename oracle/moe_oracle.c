@@ -303,6 +303,44 @@ int orc_dispatch(int R, int T, int H, int E, int k, int max_m, int dtype,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Receive side: compaction into contiguous expert-major buffers.            */
+/* ------------------------------------------------------------------------ */
+
+/* [PPLX] Dispatch: once the counts and payloads have arrived, the receiver
+ * copies the tokens into contiguous buffers, one run per expert, which become
+ * the inputs of the grouped GEMM, and keeps (source rank, expert, token) for
+ * combine. Here the filled slots are packed in (expert, source rank, position)
+ * order: region_offsets[r] = filled slots of the regions before r
+ * (r = e * R + src), region_offsets[E * R] = total; slot s lands at packed row
+ * region_offsets[s / max_m] + s % max_m. */
+int orc_region_offsets(int R, int E, int max_m, const int32_t *counts, int32_t *region_offsets) {
+  int64_t acc = 0;
+  for (int64_t r = 0; r < (int64_t)E * R; ++r) {
+    if (counts[r] < 0 || counts[r] > max_m) return ORC_EINVAL;
+    region_offsets[r] = (int32_t)acc;
+    acc += counts[r];
+  }
+  region_offsets[(int64_t)E * R] = (int32_t)acc;
+  return ORC_OK;
+}
+
+/* Packed rows of n sparse slots (as produced by orc_dispatch). */
+int orc_compact(int R, int E, int max_m, int64_t row_bytes, int nsc, const int32_t *region_offsets, int64_t n,
+                const int64_t *slot_id, const uint8_t *rows, const float *scales, const int32_t *meta,
+                int64_t n_packed, uint8_t *packed_rows, float *packed_scales, int32_t *packed_meta) {
+  for (int64_t i = 0; i < n; ++i) {
+    int64_t region = slot_id[i] / max_m;
+    if (region < 0 || region >= (int64_t)E * R) return ORC_EINVAL;
+    int64_t p = (int64_t)region_offsets[region] + slot_id[i] % max_m;
+    if (p < 0 || p >= n_packed || p >= region_offsets[region + 1]) return ORC_EINVAL;
+    memcpy(packed_rows + p * row_bytes, rows + i * row_bytes, (size_t)row_bytes);
+    for (int b = 0; b < nsc; ++b) packed_scales[p * nsc + b] = scales[i * nsc + b];
+    for (int q = 0; q < 4; ++q) packed_meta[p * 4 + q] = meta[i * 4 + q];
+  }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Synthetic experts (not part of the pages' method: a stand-in for the      */
 /* expert MLPs that run between dispatch and combine).                       */
 /* ------------------------------------------------------------------------ */

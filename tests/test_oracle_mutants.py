@@ -35,6 +35,10 @@ MUTANTS = [
      "double r = floor(a / quantum) * quantum;\n  if (r < 0x1p-6)"),
     ("e4m3 subnormal boundary", "if (e < -6) e = -6;", "if (e < -7) e = -7;"),
     ("e4m3 no saturation", "if (a >= 448.0) return (uint8_t)(sign | 0x7E);", "if (a >= 480.0) return (uint8_t)(sign | 0x7E);"),
+    ("packed offsets skip a region", "    region_offsets[r] = (int32_t)acc;\n    acc += counts[r];",
+     "    acc += counts[r];\n    region_offsets[r] = (int32_t)acc;"),
+    ("packed position ignored", "int64_t p = (int64_t)region_offsets[region] + slot_id[i] % max_m;",
+     "int64_t p = (int64_t)region_offsets[region];"),
     ("quantiser scale off", "float s = amax > 0.0f ? amax / 448.0f : 1.0f;", "float s = amax > 0.0f ? amax / 447.0f : 1.0f;"),
 ]
 
@@ -57,6 +61,7 @@ PINS = [
     lambda: pins.test_e4m3_encoder_saturates_and_round_trips(None),
     lambda: pins.test_e4m3_encoder_matches_torch(None),
     lambda: pins.test_quantize_row_properties(None),
+    lambda: pins.test_compaction_groups_each_expert_by_source_then_token(None),
 ]
 
 

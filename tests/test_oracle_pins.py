@@ -402,3 +402,28 @@ def test_dispatch_quantises_each_token_once(oracle_lib):
         q, sc = oracle.quantize_row(inp.x.reshape(12, 256)[i])
         for j in range(3):
             assert np.array_equal(sl.rows[i * 3 + j], q) and np.array_equal(sl.scales[i * 3 + j], sc)
+
+
+# --- receive side: compaction into expert-major buffers ----------------------------
+
+def test_compaction_groups_each_expert_by_source_then_token(oracle_lib):
+    """Packed rows of expert e are exactly its tokens, source rank by source rank,
+    each source's tokens in increasing order; offsets are the cumulative counts."""
+    w = wl.custom("cmp", num_ranks=3, tokens_per_rank=20, hidden=64, num_experts=6, topk=2, max_m=20)
+    inp = wl.make_inputs(w, seed=4)
+    counts, _, tok_slot = oracle.layout(inp.topk_idx, 6, 20)
+    off = oracle.region_offsets(counts, 20)
+    assert np.array_equal(off[1:], np.cumsum(counts.ravel()))             # counts in (expert, source) order
+    sl = oracle.dispatch(inp.x, None, tok_slot, 6, 20, oracle.BF16)
+    pk = oracle.compact(sl, off, 3, 6, 20, 3 * 20 * 2)
+    rows = inp.x.reshape(60, -1).view(np.uint8)
+    p = 0
+    for e in range(6):                                                      # brute force enumeration
+        for src in range(3):
+            for t in range(20):
+                if e in inp.topk_idx[src, t]:
+                    j = list(inp.topk_idx[src, t]).index(e)
+                    assert list(pk.meta[p]) == [src, t, e, j]
+                    assert np.array_equal(pk.rows[p], rows[src * 20 + t])
+                    p += 1
+    assert p == 120
