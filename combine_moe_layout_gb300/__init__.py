@@ -18,12 +18,16 @@ from ._binding import (  # noqa: F401
     MoeBuffers,
     MoeDesc,
     MoeError,
+    PackedBuffers,
     allocate_buffers,
+    allocate_packed,
     library_path,
     load,
     moe_buffer_sizes,
     moe_combine,
+    moe_combine_packed,
     moe_dispatch,
+    moe_dispatch_recv,
     moe_expert_stub,
     moe_get_error,
     moe_layout,

@@ -67,6 +67,8 @@ def load():
     lib.moe_layout.argtypes = [pdesc] + [vp] * 6
     lib.moe_dispatch.argtypes = [pdesc] + [vp] * 9
     lib.moe_layout_dispatch.argtypes = [pdesc] + [vp] * 11
+    lib.moe_dispatch_recv.argtypes = [pdesc] + [vp] * 11
+    lib.moe_combine_packed.argtypes = [pdesc] + [vp] * 8
     lib.moe_expert_stub.argtypes = [pdesc] + [vp] * 6
     lib.moe_combine.argtypes = [pdesc] + [vp] * 7
     lib.moe_reset.argtypes = [pdesc] + [vp] * 3
@@ -75,8 +77,8 @@ def load():
     lib.moe_layout_dispatch_kernels.restype = ctypes.c_int32
     lib.moe_status_string.argtypes = [ctypes.c_int32]
     lib.moe_status_string.restype = ctypes.c_char_p
-    for name in ("moe_buffer_sizes", "moe_layout", "moe_dispatch", "moe_layout_dispatch", "moe_expert_stub",
-                 "moe_combine", "moe_reset", "moe_get_error"):
+    for name in ("moe_buffer_sizes", "moe_layout", "moe_dispatch", "moe_layout_dispatch", "moe_dispatch_recv",
+                 "moe_expert_stub", "moe_combine", "moe_combine_packed", "moe_reset", "moe_get_error"):
         getattr(lib, name).restype = st
     _lib = lib
     return lib
@@ -149,6 +151,19 @@ def moe_combine(desc, expert_out, topk_weights, tok_slot, flags, out, err, strea
                               _ptr(flags), _ptr(out, True), _ptr(err), _stream(stream)), "moe_combine")
 
 
+def moe_dispatch_recv(desc, counts, flags, recv_x, recv_scales, recv_meta, region_offsets, packed_x, packed_scales,
+                      packed_meta, err, stream=None):
+    _check(load().moe_dispatch_recv(ctypes.byref(desc), _ptr(counts), _ptr(flags), _ptr(recv_x), _ptr(recv_scales),
+                                    _ptr(recv_meta), _ptr(region_offsets), _ptr(packed_x), _ptr(packed_scales),
+                                    _ptr(packed_meta), _ptr(err), _stream(stream)), "moe_dispatch_recv")
+
+
+def moe_combine_packed(desc, packed_y, region_offsets, topk_weights, tok_slot, flags, out, err, stream=None):
+    _check(load().moe_combine_packed(ctypes.byref(desc), _ptr(packed_y), _ptr(region_offsets),
+                                     _ptr(topk_weights, True), _ptr(tok_slot), _ptr(flags), _ptr(out, True),
+                                     _ptr(err), _stream(stream)), "moe_combine_packed")
+
+
 def moe_reset(desc, flags, err, stream=None):
     _check(load().moe_reset(ctypes.byref(desc), _ptr(flags), _ptr(err), _stream(stream)), "moe_reset")
 
@@ -170,6 +185,28 @@ class MoeBuffers:
     expert_out: torch.Tensor | None
     out: torch.Tensor
     err: torch.Tensor
+
+
+@dataclass
+class PackedBuffers:
+    """Outputs of moe_dispatch_recv: expert-major rows of the filled slots."""
+    region_offsets: torch.Tensor  # [E*R + 1] int32
+    packed_x: torch.Tensor        # [R*T*k, row bytes] uint8
+    packed_scales: torch.Tensor | None
+    packed_meta: torch.Tensor     # [R*T*k, 4] int32
+
+
+def allocate_packed(desc: MoeDesc, device) -> PackedBuffers:
+    R, T, H, E, k = desc.num_ranks, desc.tokens_per_rank, desc.hidden, desc.num_experts, desc.topk
+    n = max(1, R * T * k)
+    row = 2 * H if desc.dtype == MOE_BF16 else H
+    dev = torch.device(device)
+    return PackedBuffers(
+        region_offsets=torch.zeros(E * R + 1, dtype=torch.int32, device=dev),
+        packed_x=torch.empty((n, row), dtype=torch.uint8, device=dev),
+        packed_scales=torch.empty((n, H // 128), dtype=torch.float32, device=dev) if desc.dtype != MOE_BF16 else None,
+        packed_meta=torch.empty((n, 4), dtype=torch.int32, device=dev),
+    )
 
 
 def allocate_buffers(desc: MoeDesc, device, with_expert_out: bool | None = None) -> MoeBuffers:

@@ -103,5 +103,17 @@ class MoeStep:
         self.experts(stream)
         self.combine(d, stream)
 
+    def recv(self, packed: B.PackedBuffers, stream=None):
+        """The receive hook: wait for the counts, pack the filled slots expert-major."""
+        b = self.buf
+        B.moe_dispatch_recv(self.desc, b.counts, b.flags, b.recv_x, b.recv_scales, b.recv_meta, packed.region_offsets,
+                            packed.packed_x, packed.packed_scales, packed.packed_meta, b.err, stream)
+
+    def combine_packed(self, d: DeviceInputs, packed_y: torch.Tensor, region_offsets: torch.Tensor, stream=None,
+                       out=None):
+        b = self.buf
+        B.moe_combine_packed(self.desc, packed_y, region_offsets, d.topk_weights, b.tok_slot, b.flags,
+                             b.out if out is None else out, b.err, stream)
+
     def error(self, stream=None) -> int:
         return B.moe_get_error(self.buf.err, stream)

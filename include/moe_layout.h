@@ -158,6 +158,37 @@ moe_status moe_layout_dispatch(const moe_desc *desc, const int32_t *topk_idx, co
  * Host-only. */
 int32_t moe_layout_dispatch_kernels(const moe_desc *desc);
 
+/* Receive side of dispatch, the "hook" run when the experts want their inputs
+ * (Perplexity, "Dispatch": wait for every count, then copy the payloads into
+ * contiguous per-expert buffers for the grouped GEMM, keeping source rank,
+ * expert and token for combine; "NVSHMEM and DeepEP", low-latency section:
+ * receiving is a separate step after a send that only issued its writes).
+ * Waits, bounded, for every region's count + 1 flag, checks flag - 1 == count,
+ * then packs the filled slots in (expert, source rank, position) order:
+ *   region_offsets[r] = filled slots of the regions before r (r = e*R + src),
+ *   region_offsets[E*R] = total, so expert e's rows are
+ *   [region_offsets[e*R], region_offsets[(e+1)*R]); slot s lands at packed row
+ *   region_offsets[s / max_m] + s % max_m.
+ *   counts, flags, recv_x, recv_scales, recv_meta: from layout and dispatch (read).
+ *   region_offsets [E*R + 1] int32 (written).
+ *   packed_x [R*T*k] dispatched rows, 16-byte aligned; packed_scales
+ *   [R*T*k][H/128] (NULL for bf16); packed_meta [R*T*k][4] int32, 16-byte aligned
+ *   (written: the first region_offsets[E*R] rows).
+ * Device errors: a flag still zero after the bounded wait -> MOE_ETIMEOUT; a flag
+ * that disagrees with its count -> MOE_EINVAL; a count above max_m ->
+ * MOE_EOVERFLOW (clamped, so nothing is written out of bounds). */
+moe_status moe_dispatch_recv(const moe_desc *desc, const int32_t *counts, const uint64_t *flags, const void *recv_x,
+                             const float *recv_scales, const int32_t *recv_meta, int32_t *region_offsets,
+                             void *packed_x, float *packed_scales, int32_t *packed_meta, int32_t *err, void *stream);
+
+/* Combine reading the expert outputs in the packed layout of moe_dispatch_recv:
+ * the same result as moe_combine, with the output of slot s read from row
+ * region_offsets[s / max_m] + s % max_m of packed_y [R*T*k][H] bf16 (16-byte
+ * aligned). Clears the flags like moe_combine. */
+moe_status moe_combine_packed(const moe_desc *desc, const uint16_t *packed_y, const int32_t *region_offsets,
+                              const float *topk_weights, const int32_t *tok_slot, uint64_t *flags, uint16_t *out,
+                              int32_t *err, void *stream);
+
 /* Synthetic experts for tests and benchmarks (not part of the pages' method):
  * for every filled slot (pos < counts) of an fp8 or bf16-to-fp8 step,
  * expert_out = bf16_rne(e4m3(q) * scale * (1 + e/256)), the product taken

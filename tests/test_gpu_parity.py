@@ -389,3 +389,66 @@ def test_quantised_dispatch_rejects_input_scales():
     with pytest.raises(B.MoeError):
         B.moe_dispatch(step.desc, d.x, bogus, step.buf.tok_slot, step.buf.flags, step.buf.recv_x,
                        step.buf.recv_scales, step.buf.recv_meta, step.buf.err)
+
+
+# --- receive hook: compaction into expert-major buffers, and the packed combine ----
+
+def _slot_of_packed(offsets: np.ndarray, counts: np.ndarray, max_m: int) -> np.ndarray:
+    """Slot id of every packed row, from the offsets (host side, for the checks)."""
+    c = counts.ravel()
+    return np.concatenate([r * max_m + np.arange(c[r]) for r in range(c.size)]).astype(np.int64) \
+        if c.sum() else np.zeros(0, np.int64)
+
+
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+@pytest.mark.parametrize("name", ["tiny", "ds_decode", "skewed", "ds_decode_bf16in"])
+def test_recv_packs_expert_major_and_combine_reads_it(name, fused):
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w)
+    ref = oracle.run(w, inp)
+    step = P.MoeStep(w, "cuda:0")
+    d = P.to_device(inp, "cuda:0")
+    step.reset()
+    step.run(d, fused=fused)                      # slot-layout combine, the reference for the packed one
+    assert step.error() == B.MOE_OK
+    out_slots = step.buf.out.clone()
+    packed = B.allocate_packed(step.desc, "cuda:0")
+    packed.packed_meta.fill_(-7)
+    # the flags were cleared by combine: signal again and receive
+    if fused:
+        step.layout_dispatch(d)
+    else:
+        step.layout(d)
+        step.dispatch(d)
+    step.recv(packed)
+    assert step.error() == B.MOE_OK
+    off = oracle.region_offsets(ref.counts, w.max_m)
+    assert np.array_equal(packed.region_offsets.cpu().numpy(), off)
+    opk = oracle.compact(ref.slots, off, w.num_ranks, w.num_experts, w.max_m, w.num_tokens * w.topk)
+    n = int(off[-1])
+    assert n == w.num_tokens * w.topk
+    assert np.array_equal(packed.packed_meta[:n].cpu().numpy(), opk.meta)
+    assert np.array_equal(packed.packed_x[:n].cpu().numpy(), opk.rows)
+    if packed.packed_scales is not None:
+        assert np.array_equal(packed.packed_scales[:n].cpu().numpy().view(np.uint32), opk.scales.view(np.uint32))
+    # expert outputs in packed order, then the packed combine
+    y = step.y
+    sop = torch.from_numpy(_slot_of_packed(off, ref.counts, w.max_m)).cuda()
+    packed_y = y.index_select(0, sop).contiguous()
+    step.combine_packed(d, packed_y, packed.region_offsets)
+    assert step.error() == B.MOE_OK
+    assert torch.equal(step.buf.out.view(torch.int16), out_slots.view(torch.int16))
+    assert not step.buf.flags.any().item()
+
+
+def test_recv_without_counts_times_out():
+    w = wl.WORKLOADS["tiny"]
+    step = P.MoeStep(w, "cuda:0")
+    d = P.to_device(wl.make_inputs(w), "cuda:0")
+    step.reset()
+    step.layout(d)
+    step.dispatch(d)
+    step.reset()                                  # the count + 1 signals never arrive
+    packed = B.allocate_packed(step.desc, "cuda:0")
+    step.recv(packed)
+    assert step.error() == B.MOE_ETIMEOUT
