@@ -215,6 +215,20 @@ def run_native(args, rank, local_rank, world):
 
     fused = not args.unfused
     kernels = B.moe_layout_dispatch_kernels(step.desc) + 1 if fused else 3
+    packed = packed_y = None
+    if args.packed:
+        # receive hook + packed combine: expert outputs resident in packed order
+        packed = B.allocate_packed(step.desc, dev)
+        step.layout_dispatch(d)
+        step.recv(packed)
+        ts = step.buf.tok_slot.view(-1).long()
+        m = packed.packed_meta[:w.num_tokens * w.topk].long()
+        slot_of_packed = ts[(m[:, 0] * w.tokens_per_rank + m[:, 1]) * w.topk + m[:, 3]]
+        packed_y = step.y.index_select(0, slot_of_packed).contiguous()
+        step.combine_packed(d, packed_y, packed.region_offsets)
+        if step.error() != B.MOE_OK:
+            raise RuntimeError("packed step failed")
+        kernels += 2
 
     def path(dd, out=None):
         if fused:
@@ -222,7 +236,11 @@ def run_native(args, rank, local_rank, world):
         else:
             step.layout(dd)
             step.dispatch(dd)
-        step.combine(dd, out=out)
+        if packed is not None:
+            step.recv(packed)
+            step.combine_packed(dd, packed_y, packed.region_offsets, out=out)
+        else:
+            step.combine(dd, out=out)
 
     K, W = args.steps, args.warmup
     for _ in range(W):
@@ -260,7 +278,11 @@ def run_native(args, rank, local_rank, world):
     # per-kernel durations, CUDA events on the launching stream (a second pass of K steps)
     stages = [("layout_dispatch", step.layout_dispatch)] if fused else \
         [("layout", step.layout), ("dispatch", step.dispatch)]
-    stages.append(("combine", step.combine))
+    if packed is not None:
+        stages.append(("recv", lambda dd: step.recv(packed)))
+        stages.append(("combine_packed", lambda dd: step.combine_packed(dd, packed_y, packed.region_offsets)))
+    else:
+        stages.append(("combine", step.combine))
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
     for i in range(K):
         flush()
@@ -349,10 +371,13 @@ def run_native(args, rank, local_rank, world):
 
     ab = dict(w.algorithmic_bytes())
     ab["layout_dispatch"] = ab["layout"] + ab["dispatch"]
+    comb = "combine_packed" if packed is not None else "combine"
+    if packed is not None:
+        ab["total"] = ab["total_packed"]
     peak, peak_kind = measured_hbm_peak()
-    comb_s = kern_ms["combine"] / 1e3
-    achieved = ab["combine"] / comb_s / 1e9
-    traffic = profiled_traffic("moe_combine.cu", w.name)
+    comb_s = kern_ms[comb] / 1e3
+    achieved = ab[comb] / comb_s / 1e9
+    traffic = profiled_traffic("moe_combine.cu", w.name) if packed is None else None
     kernel_stats = {}
     for name in kern_ms:
         gbs = ab[name] / (kern_ms[name] / 1e3) / 1e9
@@ -384,6 +409,8 @@ def run_native(args, rank, local_rank, world):
                   "then a read of another (cold, clean L2)",
             "step_kernels": "fused layout+dispatch, combine" if fused else "layout, dispatch, combine",
             "launch": "one CUDA graph replay per step" if args.graph else "direct launches through the C ABI",
+            "receive": "receive hook packs the slots expert-major, packed combine" if packed is not None
+                       else "combine reads the fixed slots",
             "parallelism": "replicas only: one independent EP group of 8 logical ranks per GPU",
             "num_sms": args.num_sms,
         },
@@ -393,7 +420,7 @@ def run_native(args, rank, local_rank, world):
         "roofline": {"kernel": "combine_kernel", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"{peak_kind} (copy bandwidth)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": ab["combine"]},
+                     "algorithmic_bytes_per_launch": ab[comb]},
         "kernels": kernel_stats,
         "kernel_timing": "CUDA events between the launches, a second pass of the same K steps",
         "e2e": e2e,
@@ -547,6 +574,8 @@ def main(argv=None):
     ap.add_argument("--num-sms", type=int, default=0)
     ap.add_argument("--unfused", action="store_true", help="time layout and dispatch as two calls")
     ap.add_argument("--graph", action="store_true", help="replay the step's launches from a CUDA graph")
+    ap.add_argument("--packed", action="store_true",
+                    help="step = layout+dispatch, the receive hook (expert-major packing), the packed combine")
     ap.add_argument("--calibrate", action="store_true",
                     help="print the bandwidth of plain device writes and copies at the step's sizes and exit")
     ap.add_argument("--no-e2e", action="store_true")

@@ -83,7 +83,11 @@ class Workload:
         in_sc = sc if self.dtype == "fp8" else 0
         dis = N * (self.in_row_bytes + in_sc) + N * k * (self.row_bytes + sc + 16) + N * k * 4
         com = N * k * 2 * H + N * 2 * H + N * k * 4 + N * k * 4
-        return {"layout": lay, "dispatch": dis, "combine": com, "total": lay + dis + com}
+        # receive hook: read counts and flags, write the offsets, move each filled slot (row + scales + header)
+        # once into its packed row; the packed combine also reads one offset per choice
+        rcv = E * R * (4 + 8 + 4) + 2 * N * k * (self.row_bytes + sc + 16)
+        return {"layout": lay, "dispatch": dis, "combine": com, "recv": rcv, "combine_packed": com + N * k * 4,
+                "total": lay + dis + com, "total_packed": lay + dis + rcv + com + N * k * 4}
 
 
 WORKLOADS = {
