@@ -225,7 +225,7 @@ def run_native(args, rank, local_rank, world):
         m = packed.packed_meta[:w.num_tokens * w.topk].long()
         slot_of_packed = ts[(m[:, 0] * w.tokens_per_rank + m[:, 1]) * w.topk + m[:, 3]]
         packed_y = step.y.index_select(0, slot_of_packed).contiguous()
-        step.combine_packed(d, packed_y, packed.region_offsets)
+        step.combine_packed(d, packed_y, packed)
         if step.error() != B.MOE_OK:
             raise RuntimeError("packed step failed")
         kernels += 2
@@ -238,7 +238,7 @@ def run_native(args, rank, local_rank, world):
             step.dispatch(dd)
         if packed is not None:
             step.recv(packed)
-            step.combine_packed(dd, packed_y, packed.region_offsets, out=out)
+            step.combine_packed(dd, packed_y, packed, out=out)
         else:
             step.combine(dd, out=out)
 
@@ -280,7 +280,7 @@ def run_native(args, rank, local_rank, world):
         [("layout", step.layout), ("dispatch", step.dispatch)]
     if packed is not None:
         stages.append(("recv", lambda dd: step.recv(packed)))
-        stages.append(("combine_packed", lambda dd: step.combine_packed(dd, packed_y, packed.region_offsets)))
+        stages.append(("combine_packed", lambda dd: step.combine_packed(dd, packed_y, packed)))
     else:
         stages.append(("combine", step.combine))
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]

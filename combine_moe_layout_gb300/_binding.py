@@ -67,8 +67,8 @@ def load():
     lib.moe_layout.argtypes = [pdesc] + [vp] * 6
     lib.moe_dispatch.argtypes = [pdesc] + [vp] * 9
     lib.moe_layout_dispatch.argtypes = [pdesc] + [vp] * 11
-    lib.moe_dispatch_recv.argtypes = [pdesc] + [vp] * 11
-    lib.moe_combine_packed.argtypes = [pdesc] + [vp] * 8
+    lib.moe_dispatch_recv.argtypes = [pdesc] + [vp] * 12
+    lib.moe_combine_packed.argtypes = [pdesc] + [vp] * 7
     lib.moe_expert_stub.argtypes = [pdesc] + [vp] * 6
     lib.moe_combine.argtypes = [pdesc] + [vp] * 7
     lib.moe_reset.argtypes = [pdesc] + [vp] * 3
@@ -152,16 +152,16 @@ def moe_combine(desc, expert_out, topk_weights, tok_slot, flags, out, err, strea
 
 
 def moe_dispatch_recv(desc, counts, flags, recv_x, recv_scales, recv_meta, region_offsets, packed_x, packed_scales,
-                      packed_meta, err, stream=None):
+                      packed_meta, tok_packed, err, stream=None):
     _check(load().moe_dispatch_recv(ctypes.byref(desc), _ptr(counts), _ptr(flags), _ptr(recv_x), _ptr(recv_scales),
                                     _ptr(recv_meta), _ptr(region_offsets), _ptr(packed_x), _ptr(packed_scales),
-                                    _ptr(packed_meta), _ptr(err), _stream(stream)), "moe_dispatch_recv")
+                                    _ptr(packed_meta), _ptr(tok_packed), _ptr(err), _stream(stream)),
+           "moe_dispatch_recv")
 
 
-def moe_combine_packed(desc, packed_y, region_offsets, topk_weights, tok_slot, flags, out, err, stream=None):
-    _check(load().moe_combine_packed(ctypes.byref(desc), _ptr(packed_y), _ptr(region_offsets),
-                                     _ptr(topk_weights, True), _ptr(tok_slot), _ptr(flags), _ptr(out, True),
-                                     _ptr(err), _stream(stream)), "moe_combine_packed")
+def moe_combine_packed(desc, packed_y, tok_packed, topk_weights, flags, out, err, stream=None):
+    _check(load().moe_combine_packed(ctypes.byref(desc), _ptr(packed_y), _ptr(tok_packed), _ptr(topk_weights, True),
+                                     _ptr(flags), _ptr(out, True), _ptr(err), _stream(stream)), "moe_combine_packed")
 
 
 def moe_reset(desc, flags, err, stream=None):
@@ -194,6 +194,7 @@ class PackedBuffers:
     packed_x: torch.Tensor        # [R*T*k, row bytes] uint8
     packed_scales: torch.Tensor | None
     packed_meta: torch.Tensor     # [R*T*k, 4] int32
+    tok_packed: torch.Tensor      # [R, T, k] int32
 
 
 def allocate_packed(desc: MoeDesc, device) -> PackedBuffers:
@@ -206,6 +207,7 @@ def allocate_packed(desc: MoeDesc, device) -> PackedBuffers:
         packed_x=torch.empty((n, row), dtype=torch.uint8, device=dev),
         packed_scales=torch.empty((n, H // 128), dtype=torch.float32, device=dev) if desc.dtype != MOE_BF16 else None,
         packed_meta=torch.empty((n, 4), dtype=torch.int32, device=dev),
+        tok_packed=torch.empty((R, T, k), dtype=torch.int32, device=dev),
     )
 
 

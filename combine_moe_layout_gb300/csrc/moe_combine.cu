@@ -36,18 +36,9 @@ struct CombineArgs {
   uint64_t *flags;
   uint16_t *out;
   int32_t *err;
-  int H, k, nflags, chunks, early, max_m;
-  int64_t nslots;
-  // packed layout: expert output rows at region_offsets[s / max_m] + s % max_m
-  // instead of at the slot s (nullptr: the fixed-slot layout)
-  const int32_t *region_offsets;
+  int H, k, nflags, chunks, early;
+  int64_t nslots;  // rows of y: the slots (fixed-slot layout) or the packed rows
 };
-
-// Row of the expert outputs that holds slot s.
-__device__ __forceinline__ int64_t y_row(const CombineArgs &a, int32_t s) {
-  if (a.region_offsets == nullptr) return s;
-  return static_cast<int64_t>(a.region_offsets[s / a.max_m]) + s % a.max_m;
-}
 
 __device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float w, const uint4 &v) {
   const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -124,7 +115,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_tma_kernel(CombineArg
     mbar_arrive_expect_tx(&bar, nvalid * bytes);
     for (int j = 0; j < K; ++j)
       if (s_slot[j] >= 0)
-        bulk_load(&stage[j][0], a.y + y_row(a, s_slot[j]) * a.H + static_cast<int64_t>(v0) * 8, bytes, &bar);
+        bulk_load(&stage[j][0], a.y + static_cast<int64_t>(s_slot[j]) * a.H + static_cast<int64_t>(v0) * 8, bytes,
+                  &bar);
   }
   if (!mbar_wait_bounded(&bar, 0)) {
     latch_error(a.err, MOE_ETIMEOUT);
@@ -184,7 +176,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
     for (int j = 0; j < KC; ++j)
       if (j < k)
         y[u][j] = (v < V && slot[j] >= 0)
-                      ? __ldcs(reinterpret_cast<const uint4 *>(a.y + y_row(a, slot[j]) * a.H) + v)
+                      ? __ldcs(reinterpret_cast<const uint4 *>(a.y + static_cast<int64_t>(slot[j]) * a.H) + v)
                       : make_uint4(0, 0, 0, 0);
   }
   uint4 *dst = reinterpret_cast<uint4 *>(a.out + tok * a.H);
@@ -227,11 +219,10 @@ moe_status launch_combine_k(CombineArgs a, int64_t ntok, cudaStream_t stream) {
   return launch_status();
 }
 
-moe_status launch_combine(const Sizes &s, const uint16_t *y, const int32_t *region_offsets, const float *weights,
+moe_status launch_combine(const Sizes &s, const uint16_t *y, int64_t y_rows, const float *weights,
                           const int32_t *tok_slot, uint64_t *flags, uint16_t *out, int32_t *err,
                           cudaStream_t stream) {
-  CombineArgs a{y, weights, tok_slot, flags, out, err, s.H, s.k, s.E * s.R, 1, early_trigger(s.ntok), s.max_m,
-                s.nslots, region_offsets};
+  CombineArgs a{y, weights, tok_slot, flags, out, err, s.H, s.k, s.E * s.R, 1, early_trigger(s.ntok), y_rows};
   if (s.ntok == 0) {
     // nothing to gather; still clear the flags for the next step
     if (cudaMemsetAsync(flags, 0, static_cast<size_t>(s.E) * s.R * sizeof(uint64_t), stream) != cudaSuccess)
@@ -264,22 +255,22 @@ extern "C" moe_status moe_combine(const moe_desc *desc, const uint16_t *expert_o
   if (!aligned16(expert_out) || !aligned16(out) || !aligned4(topk_weights) || !aligned4(tok_slot) ||
       !aligned4(err) || (reinterpret_cast<uintptr_t>(flags) & 7u) != 0)
     return MOE_EINVAL;
-  return launch_combine(s, expert_out, nullptr, topk_weights, tok_slot, flags, out, err,
+  return launch_combine(s, expert_out, s.nslots, topk_weights, tok_slot, flags, out, err,
                         static_cast<cudaStream_t>(stream));
 }
 
-extern "C" moe_status moe_combine_packed(const moe_desc *desc, const uint16_t *packed_y, const int32_t *region_offsets,
-                                         const float *topk_weights, const int32_t *tok_slot, uint64_t *flags,
-                                         uint16_t *out, int32_t *err, void *stream) {
+extern "C" moe_status moe_combine_packed(const moe_desc *desc, const uint16_t *packed_y, const int32_t *tok_packed,
+                                         const float *topk_weights, uint64_t *flags, uint16_t *out, int32_t *err,
+                                         void *stream) {
   Sizes s;
   moe_status st = check_desc(desc, &s);
   if (st != MOE_OK) return st;
-  if (flags == nullptr || err == nullptr || region_offsets == nullptr) return MOE_EINVAL;
-  if (s.ntok > 0 && (packed_y == nullptr || topk_weights == nullptr || tok_slot == nullptr || out == nullptr))
+  if (flags == nullptr || err == nullptr) return MOE_EINVAL;
+  if (s.ntok > 0 && (packed_y == nullptr || topk_weights == nullptr || tok_packed == nullptr || out == nullptr))
     return MOE_EINVAL;
-  if (!aligned16(packed_y) || !aligned16(out) || !aligned4(topk_weights) || !aligned4(tok_slot) ||
-      !aligned4(region_offsets) || !aligned4(err) || (reinterpret_cast<uintptr_t>(flags) & 7u) != 0)
+  if (!aligned16(packed_y) || !aligned16(out) || !aligned4(topk_weights) || !aligned4(tok_packed) ||
+      !aligned4(err) || (reinterpret_cast<uintptr_t>(flags) & 7u) != 0)
     return MOE_EINVAL;
-  return launch_combine(s, packed_y, region_offsets, topk_weights, tok_slot, flags, out, err,
+  return launch_combine(s, packed_y, s.ntok * s.k, topk_weights, tok_packed, flags, out, err,
                         static_cast<cudaStream_t>(stream));
 }

@@ -15,7 +15,9 @@
 //                       of the counts in (expert, source rank) order.
 //   compact_kernel      one warp per packed row p < R*T*k: binary search of the
 //                       region holding p, then the row, its scales and its
-//                       header copied with 16-byte loads and stores. The grid is
+//                       header copied with 16-byte loads and stores, and p
+//                       recorded in tok_packed[src][t][j] (the forward map the
+//                       packed combine gathers through). The grid is
 //                       the largest possible packed size, so the host needs no
 //                       count and the call stays asynchronous.
 #include "moe_common.cuh"
@@ -93,8 +95,9 @@ struct CompactArgs {
   uint8_t *packed_x;
   float *packed_scales;
   int4 *packed_meta;
+  int32_t *tok_packed;
   int64_t nreg, npacked_max;
-  int max_m, nsc;
+  int T, k, max_m, nsc;
   uint32_t row_bytes;
 };
 
@@ -119,12 +122,19 @@ __global__ void __launch_bounds__(kCompactWarps * 32) compact_kernel(CompactArgs
   uint4 *dst = reinterpret_cast<uint4 *>(a.packed_x + p * a.row_bytes);
   for (uint32_t v = lane; v < a.row_bytes / 16; v += 32) dst[v] = __ldcs(src + v);
   for (int c = lane; c < a.nsc; c += 32) a.packed_scales[p * a.nsc + c] = a.recv_scales[slot * a.nsc + c];
-  if (lane == 0) a.packed_meta[p] = a.recv_meta[slot];
+  if (lane == 0) {
+    // the header {src, t, e, j} also gives combine its forward map to the packed row
+    const int4 m = a.recv_meta[slot];
+    a.packed_meta[p] = m;
+    if (m.y >= 0 && m.y < a.T && m.w >= 0 && m.w < a.k && m.x >= 0 && static_cast<int64_t>(m.x) * a.T * a.k < a.npacked_max)
+      a.tok_packed[(static_cast<int64_t>(m.x) * a.T + m.y) * a.k + m.w] = static_cast<int32_t>(p);
+  }
 }
 
 moe_status launch_recv(const Sizes &s, const int32_t *counts, const uint64_t *flags, const void *recv_x,
                        const float *recv_scales, const int32_t *recv_meta, int32_t *region_offsets, void *packed_x,
-                       float *packed_scales, int32_t *packed_meta, int32_t *err, cudaStream_t stream) {
+                       float *packed_scales, int32_t *packed_meta, int32_t *tok_packed, int32_t *err,
+                       cudaStream_t stream) {
   ScanArgs sa{counts, flags, region_offsets, err, static_cast<int64_t>(s.E) * s.R, s.max_m};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, 1, 1);
@@ -138,7 +148,7 @@ moe_status launch_recv(const Sizes &s, const int32_t *counts, const uint64_t *fl
   if (npacked == 0) return MOE_OK;
   CompactArgs ca{static_cast<const uint8_t *>(recv_x), recv_scales, reinterpret_cast<const int4 *>(recv_meta),
                  region_offsets, static_cast<uint8_t *>(packed_x), packed_scales,
-                 reinterpret_cast<int4 *>(packed_meta), sa.nreg, npacked, s.max_m, s.nsc,
+                 reinterpret_cast<int4 *>(packed_meta), tok_packed, sa.nreg, npacked, s.T, s.k, s.max_m, s.nsc,
                  static_cast<uint32_t>(s.row_bytes)};
   const int64_t blocks = (npacked + kCompactWarps - 1) / kCompactWarps;
   if (blocks > 0x7fffffffll) return MOE_EINVAL;
@@ -159,18 +169,19 @@ using namespace moe;
 extern "C" moe_status moe_dispatch_recv(const moe_desc *desc, const int32_t *counts, const uint64_t *flags,
                                         const void *recv_x, const float *recv_scales, const int32_t *recv_meta,
                                         int32_t *region_offsets, void *packed_x, float *packed_scales,
-                                        int32_t *packed_meta, int32_t *err, void *stream) {
+                                        int32_t *packed_meta, int32_t *tok_packed, int32_t *err, void *stream) {
   Sizes s;
   moe_status st = check_desc(desc, &s);
   if (st != MOE_OK) return st;
   if (counts == nullptr || flags == nullptr || region_offsets == nullptr || err == nullptr) return MOE_EINVAL;
-  if (s.ntok > 0 && (recv_x == nullptr || recv_meta == nullptr || packed_x == nullptr || packed_meta == nullptr))
+  if (s.ntok > 0 && (recv_x == nullptr || recv_meta == nullptr || packed_x == nullptr || packed_meta == nullptr ||
+                     tok_packed == nullptr))
     return MOE_EINVAL;
   if (s.nsc > 0 && s.ntok > 0 && (recv_scales == nullptr || packed_scales == nullptr)) return MOE_EINVAL;
   if (!aligned16(recv_x) || !aligned16(packed_x) || !aligned16(recv_meta) || !aligned16(packed_meta) ||
       !aligned4(counts) || !aligned4(region_offsets) || !aligned4(err) || !aligned4(recv_scales) ||
-      !aligned4(packed_scales) || (reinterpret_cast<uintptr_t>(flags) & 7u) != 0)
+      !aligned4(packed_scales) || !aligned4(tok_packed) || (reinterpret_cast<uintptr_t>(flags) & 7u) != 0)
     return MOE_EINVAL;
   return launch_recv(s, counts, flags, recv_x, recv_scales, recv_meta, region_offsets, packed_x, packed_scales,
-                     packed_meta, err, static_cast<cudaStream_t>(stream));
+                     packed_meta, tok_packed, err, static_cast<cudaStream_t>(stream));
 }

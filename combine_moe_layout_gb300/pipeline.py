@@ -107,12 +107,13 @@ class MoeStep:
         """The receive hook: wait for the counts, pack the filled slots expert-major."""
         b = self.buf
         B.moe_dispatch_recv(self.desc, b.counts, b.flags, b.recv_x, b.recv_scales, b.recv_meta, packed.region_offsets,
-                            packed.packed_x, packed.packed_scales, packed.packed_meta, b.err, stream)
+                            packed.packed_x, packed.packed_scales, packed.packed_meta, packed.tok_packed, b.err,
+                            stream)
 
-    def combine_packed(self, d: DeviceInputs, packed_y: torch.Tensor, region_offsets: torch.Tensor, stream=None,
+    def combine_packed(self, d: DeviceInputs, packed_y: torch.Tensor, packed: B.PackedBuffers, stream=None,
                        out=None):
         b = self.buf
-        B.moe_combine_packed(self.desc, packed_y, region_offsets, d.topk_weights, b.tok_slot, b.flags,
+        B.moe_combine_packed(self.desc, packed_y, packed.tok_packed, d.topk_weights, b.flags,
                              b.out if out is None else out, b.err, stream)
 
     def error(self, stream=None) -> int:

@@ -174,20 +174,22 @@ int32_t moe_layout_dispatch_kernels(const moe_desc *desc);
  *   packed_x [R*T*k] dispatched rows, 16-byte aligned; packed_scales
  *   [R*T*k][H/128] (NULL for bf16); packed_meta [R*T*k][4] int32, 16-byte aligned
  *   (written: the first region_offsets[E*R] rows).
+ *   tok_packed [R][T][k] int32 (written): the packed row of choice j of token t
+ *   of rank src, the map moe_combine_packed gathers through.
  * Device errors: a flag still zero after the bounded wait -> MOE_ETIMEOUT; a flag
  * that disagrees with its count -> MOE_EINVAL; a count above max_m ->
  * MOE_EOVERFLOW (clamped, so nothing is written out of bounds). */
 moe_status moe_dispatch_recv(const moe_desc *desc, const int32_t *counts, const uint64_t *flags, const void *recv_x,
                              const float *recv_scales, const int32_t *recv_meta, int32_t *region_offsets,
-                             void *packed_x, float *packed_scales, int32_t *packed_meta, int32_t *err, void *stream);
+                             void *packed_x, float *packed_scales, int32_t *packed_meta, int32_t *tok_packed,
+                             int32_t *err, void *stream);
 
 /* Combine reading the expert outputs in the packed layout of moe_dispatch_recv:
- * the same result as moe_combine, with the output of slot s read from row
- * region_offsets[s / max_m] + s % max_m of packed_y [R*T*k][H] bf16 (16-byte
- * aligned). Clears the flags like moe_combine. */
-moe_status moe_combine_packed(const moe_desc *desc, const uint16_t *packed_y, const int32_t *region_offsets,
-                              const float *topk_weights, const int32_t *tok_slot, uint64_t *flags, uint16_t *out,
-                              int32_t *err, void *stream);
+ * the same result as moe_combine, with choice j of token t of rank src read from
+ * row tok_packed[src][t][j] of packed_y [R*T*k][H] bf16 (16-byte aligned).
+ * Clears the flags like moe_combine. */
+moe_status moe_combine_packed(const moe_desc *desc, const uint16_t *packed_y, const int32_t *tok_packed,
+                              const float *topk_weights, uint64_t *flags, uint16_t *out, int32_t *err, void *stream);
 
 /* Synthetic experts for tests and benchmarks (not part of the pages' method):
  * for every filled slot (pos < counts) of an fp8 or bf16-to-fp8 step,

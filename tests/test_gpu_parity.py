@@ -431,11 +431,14 @@ def test_recv_packs_expert_major_and_combine_reads_it(name, fused):
     assert np.array_equal(packed.packed_x[:n].cpu().numpy(), opk.rows)
     if packed.packed_scales is not None:
         assert np.array_equal(packed.packed_scales[:n].cpu().numpy().view(np.uint32), opk.scales.view(np.uint32))
+    # the forward map: choice j of token t of rank src sits at packed row offsets[slot / max_m] + slot % max_m
+    ts = ref.tok_slot.astype(np.int64)
+    assert np.array_equal(packed.tok_packed.cpu().numpy(), off[ts // w.max_m] + ts % w.max_m)
     # expert outputs in packed order, then the packed combine
     y = step.y
     sop = torch.from_numpy(_slot_of_packed(off, ref.counts, w.max_m)).cuda()
     packed_y = y.index_select(0, sop).contiguous()
-    step.combine_packed(d, packed_y, packed.region_offsets)
+    step.combine_packed(d, packed_y, packed)
     assert step.error() == B.MOE_OK
     assert torch.equal(step.buf.out.view(torch.int16), out_slots.view(torch.int16))
     assert not step.buf.flags.any().item()
