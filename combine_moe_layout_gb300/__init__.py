@@ -34,5 +34,6 @@ from ._binding import (  # noqa: F401
     moe_layout_dispatch,
     moe_layout_dispatch_kernels,
     moe_reset,
+    moe_route_stats,
     moe_status_string,
 )

@@ -69,6 +69,7 @@ def load():
     lib.moe_layout_dispatch.argtypes = [pdesc] + [vp] * 11
     lib.moe_dispatch_recv.argtypes = [pdesc] + [vp] * 12
     lib.moe_combine_packed.argtypes = [pdesc] + [vp] * 7
+    lib.moe_route_stats.argtypes = [pdesc, vp, ctypes.c_int32, vp, vp, vp]
     lib.moe_expert_stub.argtypes = [pdesc] + [vp] * 6
     lib.moe_combine.argtypes = [pdesc] + [vp] * 7
     lib.moe_reset.argtypes = [pdesc] + [vp] * 3
@@ -78,7 +79,8 @@ def load():
     lib.moe_status_string.argtypes = [ctypes.c_int32]
     lib.moe_status_string.restype = ctypes.c_char_p
     for name in ("moe_buffer_sizes", "moe_layout", "moe_dispatch", "moe_layout_dispatch", "moe_dispatch_recv",
-                 "moe_expert_stub", "moe_combine", "moe_combine_packed", "moe_reset", "moe_get_error"):
+                 "moe_expert_stub", "moe_combine", "moe_combine_packed", "moe_route_stats", "moe_reset",
+                 "moe_get_error"):
         getattr(lib, name).restype = st
     _lib = lib
     return lib
@@ -162,6 +164,11 @@ def moe_dispatch_recv(desc, counts, flags, recv_x, recv_scales, recv_meta, regio
 def moe_combine_packed(desc, packed_y, tok_packed, topk_weights, flags, out, err, stream=None):
     _check(load().moe_combine_packed(ctypes.byref(desc), _ptr(packed_y), _ptr(tok_packed), _ptr(topk_weights, True),
                                      _ptr(flags), _ptr(out, True), _ptr(err), _stream(stream)), "moe_combine_packed")
+
+
+def moe_route_stats(desc, topk_idx, ranks_per_node: int, stats, err, stream=None):
+    _check(load().moe_route_stats(ctypes.byref(desc), _ptr(topk_idx, True), int(ranks_per_node), _ptr(stats),
+                                  _ptr(err), _stream(stream)), "moe_route_stats")
 
 
 def moe_reset(desc, flags, err, stream=None):

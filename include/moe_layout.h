@@ -191,6 +191,18 @@ moe_status moe_dispatch_recv(const moe_desc *desc, const int32_t *counts, const 
 moe_status moe_combine_packed(const moe_desc *desc, const uint16_t *packed_y, const int32_t *tok_packed,
                               const float *topk_weights, uint64_t *flags, uint16_t *out, int32_t *err, void *stream);
 
+/* Cross-node traffic of a routing ("NVSHMEM and DeepEP", high-throughput
+ * section: node-limited routing and per-node deduplication). With ranks grouped
+ * ranks_per_node to a node, for every source rank src:
+ *   stats[src*4 + 0] = tokens T,
+ *   stats[src*4 + 1] = choices whose expert's rank lies on another node (one copy per expert),
+ *   stats[src*4 + 2] = distinct destination ranks on other nodes, summed over tokens (per-GPU dedup),
+ *   stats[src*4 + 3] = distinct destination nodes other than its own, summed over tokens (per-node dedup).
+ *   topk_idx [R][T][k] (read, device or pinned host); stats [R][4] int64 (written, device).
+ * Device errors: an expert id outside [0, E) -> MOE_EINVAL (the choice is not counted). */
+moe_status moe_route_stats(const moe_desc *desc, const int32_t *topk_idx, int32_t ranks_per_node, int64_t *stats,
+                           int32_t *err, void *stream);
+
 /* Synthetic experts for tests and benchmarks (not part of the pages' method):
  * for every filled slot (pos < counts) of an fp8 or bf16-to-fp8 step,
  * expert_out = bf16_rne(e4m3(q) * scale * (1 + e/256)), the product taken

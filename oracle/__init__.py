@@ -88,6 +88,8 @@ def _bind(path: str):
     lib.orc_region_offsets.restype = i32
     lib.orc_compact.argtypes = [i32, i32, i32, i64, i32, vp, i64, vp, vp, vp, vp, i64, vp, vp, vp]
     lib.orc_compact.restype = i32
+    lib.orc_route_stats.argtypes = [i32] * 5 + [vp, vp]
+    lib.orc_route_stats.restype = i32
     lib.orc_validate.argtypes = [i32] * 7
     lib.orc_validate.restype = i32
     lib.orc_buffer_sizes.argtypes = [i32] * 7 + [vp]
@@ -268,6 +270,15 @@ def region_offsets(counts: np.ndarray, max_m: int) -> np.ndarray:
     E, R = c.shape
     out = np.zeros(E * R + 1, np.int32)
     _check(_load().orc_region_offsets(R, E, max_m, _p(c), _p(out)), "region_offsets")
+    return out
+
+
+def route_stats(topk_idx: np.ndarray, num_experts: int, ranks_per_node: int) -> np.ndarray:
+    """int64 [R][4]: tokens and cross-node copies per expert / per destination rank / per destination node."""
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    R, T, k = idx.shape
+    out = np.zeros((R, 4), np.int64)
+    _check(_load().orc_route_stats(R, T, num_experts, k, ranks_per_node, _p(idx), _p(out)), "route_stats")
     return out
 
 

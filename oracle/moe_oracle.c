@@ -341,6 +341,48 @@ int orc_compact(int R, int E, int max_m, int64_t row_bytes, int nsc, const int32
 }
 
 /* ------------------------------------------------------------------------ */
+/* Cross-node traffic of a routing (per-node deduplication accounting).      */
+/* ------------------------------------------------------------------------ */
+
+/* [NVDE] high-throughput section: a token of a GPU on node n goes to the nodes of
+ * its k experts; counting the copies that leave node n per expert, per distinct
+ * destination GPU, or per distinct destination node (DeepEP's per-node
+ * deduplication) gives the cross-node traffic of the three schemes. Ranks are
+ * grouped ranks_per_node to a node; expert e lives on rank e / (E / R).
+ * stats[src * 4 + 0..3] = tokens, per-expert, per-rank, per-node copies of
+ * source rank src, summed over its tokens. */
+int orc_route_stats(int R, int T, int E, int k, int ranks_per_node, const int32_t *topk_idx, int64_t *stats) {
+  if (ranks_per_node < 1 || E % R != 0) return ORC_EINVAL;
+  int L = E / R;
+  for (int src = 0; src < R; ++src) {
+    int64_t per_expert = 0, per_rank = 0, per_node = 0;
+    int home = src / ranks_per_node;
+    for (int t = 0; t < T; ++t) {
+      const int32_t *row = topk_idx + ((int64_t)src * T + t) * k;
+      for (int j = 0; j < k; ++j) {
+        if (row[j] < 0 || row[j] >= E) return ORC_EINVAL;
+        int rank = row[j] / L, node = rank / ranks_per_node;
+        if (node == home) continue;
+        per_expert += 1;
+        int seen_rank = 0, seen_node = 0; /* first choice with this rank / node? */
+        for (int jj = 0; jj < j; ++jj) {
+          int r2 = row[jj] / L;
+          if (r2 == rank) seen_rank = 1;
+          if (r2 / ranks_per_node == node) seen_node = 1;
+        }
+        per_rank += !seen_rank;
+        per_node += !seen_node;
+      }
+    }
+    stats[src * 4 + 0] = T;
+    stats[src * 4 + 1] = per_expert;
+    stats[src * 4 + 2] = per_rank;
+    stats[src * 4 + 3] = per_node;
+  }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Synthetic experts (not part of the pages' method: a stand-in for the      */
 /* expert MLPs that run between dispatch and combine).                       */
 /* ------------------------------------------------------------------------ */

@@ -455,3 +455,39 @@ def test_recv_without_counts_times_out():
     packed = B.allocate_packed(step.desc, "cuda:0")
     step.recv(packed)
     assert step.error() == B.MOE_ETIMEOUT
+
+
+
+# --- cross-node traffic accounting ---------------------------------------------------
+
+@pytest.mark.parametrize("name,rpn", [("ds_prefill", 2), ("ds_decode", 4), ("skewed", 4), ("tiny", 1)])
+def test_route_stats_match_the_oracle(name, rpn):
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w)
+    ref = oracle.route_stats(inp.topk_idx, w.num_experts, rpn)
+    desc = B.MoeDesc.of(w)
+    stats = torch.zeros((w.num_ranks, 4), dtype=torch.int64, device="cuda:0")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    B.moe_route_stats(desc, torch.from_numpy(inp.topk_idx).cuda(), rpn, stats, err)
+    assert B.moe_get_error(err) == B.MOE_OK
+    assert np.array_equal(stats.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("limited,key", [(False, "unlimited"), (True, "node_limited")])
+def test_route_stats_reproduce_the_printed_copies_on_the_gpu(limited, key):
+    import json
+    import os
+    import test_workloads as tw
+    want = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "node_limited_routing.json")))
+    want = want["printed"][key]
+    idx, R, gpn, E, k = tw._page_routing(limited)
+    full = np.repeat(idx[None], R, axis=0)
+    desc = B.MoeDesc(R, idx.shape[0], 128, E, k, idx.shape[0], B.MOE_BF16, 0)
+    stats = torch.zeros((R, 4), dtype=torch.int64, device="cuda:0")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    B.moe_route_stats(desc, torch.from_numpy(full).cuda(), gpn, stats, err)
+    assert B.moe_get_error(err) == B.MOE_OK
+    st = stats[0].cpu().numpy()
+    assert f"{st[1] / st[0]:.2f}" == want["per_expert"]
+    assert f"{st[2] / st[0]:.2f}" == want["per_gpu_dedup"]
+    assert f"{st[3] / st[0]:.2f}" == want["per_node_dedup"]

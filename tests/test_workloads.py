@@ -113,3 +113,34 @@ def test_algorithmic_bytes_of_the_decode_step():
     assert b["dispatch"] == N * row + N * k * (row + 16) + N * k * 4
     assert b["combine"] == N * k * 2 * H + N * 2 * H + N * k * 8
     assert 195e6 < b["total"] < 205e6
+
+
+def _page_routing(limited: bool):
+    """The page's simulation as a routing of 64 ranks (8 nodes of 8): rank 0 holds the page's 4096 tokens."""
+    g = json.load(open(os.path.join(GOLDEN, "node_limited_routing.json")))["setup"]
+    nodes, gpn, E, k, keep, tokens = g["nodes"], g["gpus_per_node"], g["experts"], g["topk"], g["max_nodes"], \
+        g["tokens"]
+    rng = np.random.default_rng(0)
+    scores = rng.random((tokens, E)) + rng.random(E) * 0.5
+    if limited:
+        idx = wl.group_limited_choice(scores, k, groups=nodes, keep_groups=keep, per_group_top=k // keep)
+    else:
+        idx = np.argsort(-scores, axis=1)[:, :k]
+    return idx.astype(np.int32), nodes * gpn, gpn, E, k
+
+
+@pytest.mark.parametrize("limited,key", [(False, "unlimited"), (True, "node_limited")])
+def test_oracle_route_stats_reproduce_the_printed_copies(limited, key):
+    """The oracle's per-node deduplication accounting gives the page's copies per token."""
+    import oracle
+    want = json.load(open(os.path.join(GOLDEN, "node_limited_routing.json")))["printed"][key]
+    idx, R, gpn, E, k = _page_routing(limited)
+    # a 64-rank job (E/R = 4 experts per rank); rank 0 holds the page's tokens
+    full = np.zeros((R, idx.shape[0], k), np.int32)
+    full[0] = idx
+    full[1:] = idx[None]                                    # other ranks: same choices (only rank 0 is read)
+    st = oracle.route_stats(full, E, gpn)[0]
+    n = st[0]
+    assert f"{st[1] / n:.2f}" == want["per_expert"]
+    assert f"{st[2] / n:.2f}" == want["per_gpu_dedup"]
+    assert f"{st[3] / n:.2f}" == want["per_node_dedup"]
