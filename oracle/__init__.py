@@ -90,6 +90,8 @@ def _bind(path: str):
     lib.orc_compact.restype = i32
     lib.orc_route_stats.argtypes = [i32] * 5 + [vp, vp]
     lib.orc_route_stats.restype = i32
+    lib.orc_expert_mlp_row.argtypes = [i32, i32] + [vp] * 6
+    lib.orc_expert_mlp_row.restype = None
     lib.orc_validate.argtypes = [i32] * 7
     lib.orc_validate.restype = i32
     lib.orc_buffer_sizes.argtypes = [i32] * 7 + [vp]
@@ -280,6 +282,19 @@ def route_stats(topk_idx: np.ndarray, num_experts: int, ranks_per_node: int) -> 
     out = np.zeros((R, 4), np.int64)
     _check(_load().orc_route_stats(R, T, num_experts, k, ranks_per_node, _p(idx), _p(out)), "route_stats")
     return out
+
+
+def expert_mlp_row(x_bits: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray, w_down: np.ndarray):
+    """bf16 bits of h [I] and y [H] of one row through one expert (SwiGLU MLP, fp64 sums)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    wg = np.ascontiguousarray(w_gate, dtype=np.uint16)
+    wu = np.ascontiguousarray(w_up, dtype=np.uint16)
+    wd = np.ascontiguousarray(w_down, dtype=np.uint16)
+    I, H = wg.shape
+    h = np.zeros(I, np.uint16)
+    y = np.zeros(H, np.uint16)
+    _load().orc_expert_mlp_row(H, I, _p(x), _p(wg), _p(wu), _p(wd), _p(h), _p(y))
+    return h, y
 
 
 @dataclass

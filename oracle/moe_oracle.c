@@ -30,6 +30,9 @@
  *
  * Floating point: fp64 throughout; the only rounding the pages fix is that
  * combine returns BF16 ([NVDE] high-throughput section), done once at the end.
+ * The expert stage ([HGT] section 7, Mega MoE: linear 1, SwiGLU, linear 2)
+ * rounds its intermediate h and its output y to bf16 once each, the precision
+ * the rows are stored in between the steps.
  *
  * parity pins: see the tests (brute force, invariants, closed forms, the
  * pages' printed buffer sizes, and library conversions).
@@ -338,6 +341,37 @@ int orc_compact(int R, int E, int max_m, int64_t row_bytes, int nsc, const int32
     for (int q = 0; q < 4; ++q) packed_meta[p * 4 + q] = meta[i * 4 + q];
   }
   return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The expert stage (an expert MLP with SwiGLU) on packed rows.              */
+/* ------------------------------------------------------------------------ */
+
+/* "How GPUs Talk to Each Other During LLM Inference", section 7 (Mega MoE):
+ * between dispatch and combine every expert runs linear 1, SwiGLU and linear 2
+ * on its tokens. For one bf16 row x of expert e, with weights of that expert in
+ * bf16 (w_gate, w_up [I][H], w_down [H][I], each row the K dimension):
+ *   h[i] = bf16( silu(sum_h x[h] w_gate[i][h]) * sum_h x[h] w_up[i][h] ),
+ *   silu(g) = g / (1 + exp(-g)),
+ *   y[j] = bf16( sum_i h[i] w_down[j][i] ),
+ * sums and silu in fp64, h rounded to bf16 once (as it is stored between the two
+ * linears), y rounded once. */
+void orc_expert_mlp_row(int H, int I, const uint16_t *x, const uint16_t *w_gate, const uint16_t *w_up,
+                        const uint16_t *w_down, uint16_t *h, uint16_t *y) {
+  for (int i = 0; i < I; ++i) {
+    double g = 0.0, u = 0.0;
+    for (int k = 0; k < H; ++k) {
+      double xv = orc_bf16_value(x[k]);
+      g += xv * orc_bf16_value(w_gate[(int64_t)i * H + k]);
+      u += xv * orc_bf16_value(w_up[(int64_t)i * H + k]);
+    }
+    h[i] = orc_bf16_from_double(g / (1.0 + exp(-g)) * u);
+  }
+  for (int j = 0; j < H; ++j) {
+    double acc = 0.0;
+    for (int i = 0; i < I; ++i) acc += orc_bf16_value(h[i]) * orc_bf16_value(w_down[(int64_t)j * I + i]);
+    y[j] = orc_bf16_from_double(acc);
+  }
 }
 
 /* ------------------------------------------------------------------------ */

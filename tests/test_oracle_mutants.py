@@ -39,6 +39,13 @@ MUTANTS = [
      "    acc += counts[r];\n    region_offsets[r] = (int32_t)acc;"),
     ("packed position ignored", "int64_t p = (int64_t)region_offsets[region] + slot_id[i] % max_m;",
      "int64_t p = (int64_t)region_offsets[region];"),
+    ("silu on the up projection", "h[i] = orc_bf16_from_double(g / (1.0 + exp(-g)) * u);",
+     "h[i] = orc_bf16_from_double(u / (1.0 + exp(-u)) * g);"),
+    ("silu sign", "g / (1.0 + exp(-g))", "g / (1.0 + exp(g))"),
+    ("gate weight transposed", "g += xv * orc_bf16_value(w_gate[(int64_t)i * H + k]);",
+     "g += xv * orc_bf16_value(w_gate[(int64_t)k * I + i]);"),
+    ("down weight transposed", "acc += orc_bf16_value(h[i]) * orc_bf16_value(w_down[(int64_t)j * I + i]);",
+     "acc += orc_bf16_value(h[i]) * orc_bf16_value(w_down[(int64_t)i * H + j]);"),
     ("quantiser scale off", "float s = amax > 0.0f ? amax / 448.0f : 1.0f;", "float s = amax > 0.0f ? amax / 447.0f : 1.0f;"),
 ]
 
@@ -62,6 +69,8 @@ PINS = [
     lambda: pins.test_e4m3_encoder_matches_torch(None),
     lambda: pins.test_quantize_row_properties(None),
     lambda: pins.test_compaction_groups_each_expert_by_source_then_token(None),
+    lambda: pins.test_expert_mlp_row_is_zero_for_zero_gate(None),
+    lambda: pins.test_expert_mlp_row_matches_a_library_matmul(None),
 ]
 
 

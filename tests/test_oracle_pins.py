@@ -427,3 +427,42 @@ def test_compaction_groups_each_expert_by_source_then_token(oracle_lib):
                     assert np.array_equal(pk.rows[p], rows[src * 20 + t])
                     p += 1
     assert p == 120
+
+
+# --- the expert stage: SwiGLU MLP of one row ------------------------------------
+
+def _bf16(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _val(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def test_expert_mlp_row_matches_a_library_matmul(oracle_lib):
+    """h and y agree with numpy's fp64 matmuls and torch's silu, with the same two bf16 roundings."""
+    rng = np.random.default_rng(30)
+    H, I = 64, 96
+    x = _bf16(rng.standard_normal(H))
+    wg, wu, wd = (_bf16(rng.standard_normal(sh) * 0.1) for sh in ((I, H), (I, H), (H, I)))
+    h, y = oracle.expert_mlp_row(x, wg, wu, wd)
+    g = _val(wg).reshape(I, H) @ _val(x)
+    u = _val(wu).reshape(I, H) @ _val(x)
+    hf = torch.nn.functional.silu(torch.from_numpy(g)).numpy() * u
+    hb = torch.from_numpy(hf.astype(np.float32)).to(torch.bfloat16).double().numpy()   # float32 first: see below
+    # the oracle rounds the fp64 value once; compare values, allowing the float32 step of the library route
+    assert (np.abs(_val(h) - hf) <= np.abs(hf) * 2.0 ** -8 * 1.0001).all()
+    assert (np.abs(_val(h) - hb) <= np.abs(hb) * 2.0 ** -7).all()
+    yf = _val(wd).reshape(H, I) @ _val(h)
+    assert (np.abs(_val(y) - yf) <= np.abs(yf) * 2.0 ** -8 * 1.0001).all()
+
+
+def test_expert_mlp_row_is_zero_for_zero_gate(oracle_lib):
+    """silu(0) = 0: a zero gate weight matrix gives h = 0 and y = 0 exactly."""
+    rng = np.random.default_rng(31)
+    H, I = 32, 48
+    x = _bf16(rng.standard_normal(H))
+    h, y = oracle.expert_mlp_row(x, np.zeros((I, H), np.uint16), _bf16(rng.standard_normal((I, H))),
+                                 _bf16(rng.standard_normal((H, I))))
+    assert ((h & 0x7FFF) == 0).all()                     # silu(0) * u is -0 where u < 0
+    assert ((y & 0x7FFF) == 0).all()
