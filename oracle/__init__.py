@@ -92,6 +92,8 @@ def _bind(path: str):
     lib.orc_route_stats.restype = i32
     lib.orc_expert_mlp_row.argtypes = [i32, i32] + [vp] * 6
     lib.orc_expert_mlp_row.restype = None
+    lib.orc_linear_row.argtypes = [i32, i32, vp, vp, vp]
+    lib.orc_linear_row.restype = None
     lib.orc_validate.argtypes = [i32] * 7
     lib.orc_validate.restype = i32
     lib.orc_buffer_sizes.argtypes = [i32] * 7 + [vp]
@@ -295,6 +297,16 @@ def expert_mlp_row(x_bits: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray, w_d
     y = np.zeros(H, np.uint16)
     _load().orc_expert_mlp_row(H, I, _p(x), _p(wg), _p(wu), _p(wd), _p(h), _p(y))
     return h, y
+
+
+def linear_row(x_bits: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """bf16 bits of y [N] = x [K] through the bf16 weight matrix w [N][K] (fp64 sum, one rounding)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    wm = np.ascontiguousarray(w, dtype=np.uint16)
+    N, K = wm.shape
+    y = np.zeros(N, np.uint16)
+    _load().orc_linear_row(K, N, _p(x), _p(wm), _p(y))
+    return y
 
 
 @dataclass

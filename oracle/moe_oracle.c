@@ -356,6 +356,17 @@ int orc_compact(int R, int E, int max_m, int64_t row_bytes, int nsc, const int32
  *   y[j] = bf16( sum_i h[i] w_down[j][i] ),
  * sums and silu in fp64, h rounded to bf16 once (as it is stored between the two
  * linears), y rounded once. */
+/* One row through one bf16 linear map: y[n] = bf16( sum_k x[k] w[n][k] ) for a
+ * weight matrix w [N][K] (each row one output, K contiguous), fp64 sum. This is
+ * linear 2 of the expert stage on its own. */
+void orc_linear_row(int K, int N, const uint16_t *x, const uint16_t *w, uint16_t *y) {
+  for (int n = 0; n < N; ++n) {
+    double acc = 0.0;
+    for (int k = 0; k < K; ++k) acc += orc_bf16_value(x[k]) * orc_bf16_value(w[(int64_t)n * K + k]);
+    y[n] = orc_bf16_from_double(acc);
+  }
+}
+
 void orc_expert_mlp_row(int H, int I, const uint16_t *x, const uint16_t *w_gate, const uint16_t *w_up,
                         const uint16_t *w_down, uint16_t *h, uint16_t *y) {
   for (int i = 0; i < I; ++i) {

@@ -46,6 +46,8 @@ MUTANTS = [
      "g += xv * orc_bf16_value(w_gate[(int64_t)k * I + i]);"),
     ("down weight transposed", "acc += orc_bf16_value(h[i]) * orc_bf16_value(w_down[(int64_t)j * I + i]);",
      "acc += orc_bf16_value(h[i]) * orc_bf16_value(w_down[(int64_t)i * H + j]);"),
+    ("linear weight transposed", "acc += orc_bf16_value(x[k]) * orc_bf16_value(w[(int64_t)n * K + k]);",
+     "acc += orc_bf16_value(x[k]) * orc_bf16_value(w[(int64_t)k * N + n]);"),
     ("quantiser scale off", "float s = amax > 0.0f ? amax / 448.0f : 1.0f;", "float s = amax > 0.0f ? amax / 447.0f : 1.0f;"),
 ]
 
@@ -71,6 +73,7 @@ PINS = [
     lambda: pins.test_compaction_groups_each_expert_by_source_then_token(None),
     lambda: pins.test_expert_mlp_row_is_zero_for_zero_gate(None),
     lambda: pins.test_expert_mlp_row_matches_a_library_matmul(None),
+    lambda: pins.test_linear_row_matches_a_library_matmul_and_an_identity(None),
 ]
 
 

@@ -466,3 +466,19 @@ def test_expert_mlp_row_is_zero_for_zero_gate(oracle_lib):
                                  _bf16(rng.standard_normal((H, I))))
     assert ((h & 0x7FFF) == 0).all()                     # silu(0) * u is -0 where u < 0
     assert ((y & 0x7FFF) == 0).all()
+
+
+def test_linear_row_matches_a_library_matmul_and_an_identity(oracle_lib):
+    """y = x W^T within one bf16 rounding of numpy's fp64 product; the identity matrix returns x."""
+    rng = np.random.default_rng(32)
+    K, N = 80, 48
+    x = _bf16(rng.standard_normal(K))
+    w = _bf16(rng.standard_normal((N, K)) * 0.1)
+    y = oracle.linear_row(x, w)
+    yf = _val(w).reshape(N, K) @ _val(x)
+    assert (np.abs(_val(y) - yf) <= np.abs(yf) * 2.0 ** -8 * 1.0001).all()
+    eye = _bf16(np.eye(K))
+    assert (oracle.linear_row(x, eye) == x).all()
+    # a permutation matrix permutes
+    perm = rng.permutation(K)
+    assert (oracle.linear_row(x, _bf16(np.eye(K)[perm])) == x[perm]).all()
