@@ -1,0 +1,542 @@
+// Expert stage between dispatch and combine: every expert's packed bf16 rows go
+// through linear 1 with SwiGLU and then linear 2, on the 5th-generation tensor
+// cores (tcgen05.mma with the accumulator in tensor memory, operands staged by
+// TMA).
+//
+// "How GPUs Talk to Each Other During LLM Inference", section 7 (Mega MoE):
+// between dispatch and combine every expert applies linear 1, SwiGLU and
+// linear 2 to the tokens it received. Perplexity, "Efficient and portable
+// mixture-of-experts communication", section "Dispatch": the receive side packs
+// each expert's tokens contiguously so that they feed a grouped GEMM. The packed
+// rows of expert e are rows [off[e*R], off[(e+1)*R]) of the buffers the receive
+// hook writes, and one grouped-GEMM kernel runs each linear map:
+//
+//   gate/up:  h[p][i] = bf16( silu(x_p . w_gate[e][i]) * (x_p . w_up[e][i]) )
+//   down:     y[p][j] = bf16( h_p . w_down[e][j] )
+//
+// bf16 operands, fp32 accumulation, silu(g) = g / (1 + exp(-g)) in fp32.
+//
+// Kernel shape: one persistent CTA per SM, 192 threads.
+//   warp 0      TMA producer: per 64-wide K block, a 128-row A tile and a
+//               256-row (or 128-row) B tile, 128-byte swizzle, into a 4-stage
+//               shared-memory ring.
+//   warp 1      owns 512 TMEM columns (two 128 x 256 fp32 accumulators, so the
+//               epilogue of one tile overlaps the MMAs of the next) and issues
+//               tcgen05.mma (M = 128, N = 256 or 128, K = 16) from one lane.
+//   warps 2-5   epilogue: each warp reads its 32-lane quarter of the
+//               accumulator with tcgen05.ld, applies SwiGLU or plain bf16
+//               rounding and stores the rows that belong to the tile's expert.
+// A tile is up to 128 consecutive packed rows of one expert. For gate/up its
+// 256 accumulator columns are 128 gate rows i0..i0+127 of the expert's weights
+// followed by the 128 up rows of the same i, so SwiGLU pairs columns c and
+// c + 128 of a thread's own row. Tiles are numbered expert by expert, n-tile by
+// n-tile, with the m-tiles innermost: CTAs that run at the same time share one
+// expert's weight tile through L2.
+//
+// Every wait is bounded: a timeout records MOE_ETIMEOUT, every role of the CTA
+// stops, the loads and MMAs already issued are waited for (again bounded) and
+// the tensor memory is freed before the CTA exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+
+#include "moe_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;            // rows of a tile (tcgen05 M)
+constexpr int kBK = 64;             // K elements per stage: one 128-byte swizzled row
+constexpr int kUK = 16;             // K of one tcgen05.mma kind::f16
+constexpr int kBNMax = 256;         // accumulator columns of a tile
+constexpr int kBoxRows = 128;       // rows of one TMA box
+constexpr int kStages = 4;
+constexpr int kTileA = kBM * kBK * 2;
+constexpr int kTileB = kBNMax * kBK * 2;
+constexpr int kStage = kTileA + kTileB;
+constexpr int kBoxBytes = kBoxRows * kBK * 2;
+constexpr int kGemmThreads = 192;
+constexpr uint32_t kTmemCols = 2 * kBNMax;
+constexpr int kSmemFixed = 1024 + kStages * kStage + (2 * kStages + 5) * 8 + 8;
+constexpr int kSmemMax = 227 * 1024;
+
+// tcgen05 shared-memory matrix descriptor of a K-major bf16 tile as TMA writes
+// it with the 128-byte swizzle: 128-byte rows (64 elements), 8-row groups 1024
+// bytes apart. Fields: start address >> 4 (bits 0-13); leading-dimension byte
+// offset >> 4 (bits 16-29; unused by swizzled K-major layouts, 1 by
+// convention); stride-dimension byte offset >> 4 (bits 32-45); descriptor
+// version 1 (bits 46-48); base offset 0 (bits 49-51: tiles start on 1024-byte
+// boundaries); swizzle mode 2 = 128 bytes (bits 61-63).
+__host__ __device__ constexpr uint64_t sw128_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(16 >> 4) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A and
+// B bf16 (bits 7-9 = 1, bits 10-12 = 1), no negation, both K-major (bits 15 and
+// 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+static_assert(sw128_desc(0x400) == ((2ull << 61) | (1ull << 46) | (64ull << 32) | (1ull << 16) | 0x40ull), "");
+static_assert(sw128_desc(0x3FC00 + 96) == ((2ull << 61) | (1ull << 46) | (64ull << 32) | (1ull << 16) | 0x3FC6ull), "");
+static_assert(idesc_bf16(128, 256) == 0x08400490u, "");
+static_assert(idesc_bf16(128, 128) == 0x08200490u, "");
+static_assert(kTileA % 1024 == 0 && kStage % 1024 == 0 && kBoxBytes % 1024 == 0, "tiles on 1024-byte boundaries");
+static_assert(kBK * 2 == 128, "one K block is one 128-byte swizzle row");
+static_assert(kSmemFixed + 8 * 2 <= kSmemMax, "");
+
+// ---------------------------------------------------------------------------
+// TMA tensor loads, tensor memory and tcgen05.mma.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D (tmem) = A * B^T (+ D when accumulate != 0), both operands K-major in shared memory.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the mbarrier when every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// tcgen05.ld of 32 consecutive fp32 columns of this thread's accumulator row
+// (32x32b shape: lane l of the warp reads TMEM lane base + l), then the wait;
+// the wait sits in the same asm block so no use of r can move above it.
+__device__ __forceinline__ void tmem_load32_wait(uint32_t taddr0, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr0)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_load32x2_wait(uint32_t taddr0, uint32_t taddr1, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr0), "r"(taddr1)
+      : "memory");
+}
+
+// Bounded wait on an mbarrier phase that also gives up as soon as another role
+// of the CTA has aborted; a timeout records MOE_ETIMEOUT and aborts the CTA.
+__device__ __forceinline__ bool role_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int32_t *err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kMbarWaitNs) {
+      *abort = 1;
+      latch_error(err, MOE_ETIMEOUT);
+      return false;
+    }
+  }
+}
+
+struct GemmArgs {
+  const int32_t *region_offsets;  // [E*R + 1] packed-row offsets of the (expert, source rank) regions
+  int32_t *err;
+  __nv_bfloat16 *out;             // [rows][n_total]
+  int rows;                       // rows of A and of out
+  int E, R;
+  int K;                          // contraction length: a multiple of 64
+  int n_total;                    // output columns of a row (I for gate/up, H for down)
+  int b_rows;                     // weight rows in one B tile: 256 (two boxes) or 128 (one box)
+  int out_cols;                   // output columns of one tile: 128 (gate/up) or b_rows (down)
+  int ntiles_n;                   // n_total / out_cols
+  int expert_rows;                // weight rows of one expert in the tensor maps (I or H)
+  int swiglu;                     // 1: gate/up tile with the SwiGLU epilogue
+};
+
+struct Tile {
+  int e, row0, rows, n0;
+};
+
+// Tile w of the CTA's sequence: its expert (pref[e] <= w < pref[e + 1]), then
+// n-tile and m-tile with the m-tiles innermost.
+__device__ __forceinline__ Tile tile_of(int w, const int32_t *pref, const int32_t *offs, const GemmArgs &a) {
+  int lo = 0, hi = a.E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] <= w)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  Tile t;
+  t.e = lo;
+  const int m = offs[lo + 1] - offs[lo];
+  const int mtiles = (m + kBM - 1) / kBM;
+  const int local = w - pref[lo];
+  const int nt = local / mtiles, mt = local - nt * mtiles;
+  t.row0 = offs[lo] + mt * kBM;
+  t.rows = min(kBM, m - mt * kBM);
+  t.n0 = nt * a.out_cols;
+  return t;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
+                        const __grid_constant__ CUtensorMap map_b1, const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + (((smem_addr(smem_raw) + 1023u) & ~1023u) - smem_addr(smem_raw));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStage);
+  uint64_t *empty = full + kStages;
+  uint64_t *tfull = empty + kStages;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *done = tempty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+  volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int32_t *offs = reinterpret_cast<int32_t *>(tmem_slot + 2);
+  int32_t *pref = offs + (a.E + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull + b, 1);
+      mbar_init(tempty + b, 4);
+    }
+    mbar_init(done, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (tid == 32) {
+    prefetch_tensormap(&map_a);
+    prefetch_tensormap(&map_b0);
+    prefetch_tensormap(&map_b1);
+  }
+  // the offsets and rows come from the previous kernel; tensor memory is only
+  // claimed once that kernel has finished
+  grid_dependency_wait();
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  for (int e = tid; e <= a.E; e += kGemmThreads) offs[e] = a.region_offsets[static_cast<int64_t>(e) * a.R];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // tiles per expert and their prefix; an expert whose rows are not a valid
+  // range of the packed buffer gets none and latches MOE_EINVAL
+  if (warp == 0) {
+    int run = 0;
+    bool bad = false;
+    for (int e0 = 0; e0 < a.E; e0 += 32) {
+      const int e = e0 + lane;
+      int tiles = 0;
+      if (e < a.E) {
+        const int lo = offs[e], hi = offs[e + 1];
+        if (lo < 0 || hi < lo || hi > a.rows)
+          bad = true;
+        else
+          tiles = ((hi - lo + kBM - 1) / kBM) * a.ntiles_n;
+      }
+      int incl = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (e < a.E) pref[e] = run + incl - tiles;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) pref[a.E] = run;
+    if (__any_sync(0xffffffffu, bad) && lane == 0) latch_error(a.err, MOE_EINVAL);
+  }
+  __syncthreads();
+  const int total = pref[a.E];
+  const int kblocks = a.K / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer ----
+      uint32_t it = 0;  // K blocks issued
+      const uint32_t bytes = kTileA + a.b_rows * kBK * 2;
+      bool ok = true;
+      for (int w = blockIdx.x; ok && w < total; w += gridDim.x) {
+        const Tile t = tile_of(w, pref, offs, a);
+        const int brow = t.e * a.expert_rows + t.n0;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+          if (!role_wait(empty + s, ph ^ 1u, abort, a.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_addr(smem + s * kStage), sb = sa + kTileA, fb = smem_addr(full + s);
+          mbar_arrive_expect_tx(full + s, bytes);
+          tma_load_2d(sa, &map_a, kb * kBK, t.row0, fb);
+          if (a.swiglu) {
+            tma_load_2d(sb, &map_b0, kb * kBK, brow, fb);
+            tma_load_2d(sb + kBoxBytes, &map_b1, kb * kBK, brow, fb);
+          } else {
+            tma_load_2d(sb, &map_b0, kb * kBK, brow, fb);
+            if (a.b_rows > kBoxRows) tma_load_2d(sb + kBoxBytes, &map_b0, kb * kBK, brow + kBoxRows, fb);
+          }
+          ++it;
+        }
+      }
+      // the last load issued into each stage lands before the CTA may exit
+      for (uint32_t s = 0; s < kStages && s < it; ++s) {
+        const uint32_t last = s + ((it - 1 - s) / kStages) * kStages;
+        mbar_wait_bounded(full + s, (last / kStages) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer ----
+      uint32_t it = 0;
+      int lt = 0;
+      const uint32_t idesc = idesc_bf16(kBM, a.b_rows);
+      bool ok = true;
+      for (int w = blockIdx.x; ok && w < total; w += gridDim.x, ++lt) {
+        const int buf = lt & 1;
+        const uint32_t ph = (lt >> 1) & 1;
+        if (!role_wait(tempty + buf, ph ^ 1u, abort, a.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * kBNMax;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const uint32_t s = it % kStages, sph = (it / kStages) & 1u;
+          if (!role_wait(full + s, sph, abort, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_addr(smem + s * kStage), sb = sa + kTileA;
+#pragma unroll
+          for (int kk = 0; kk < kBK / kUK; ++kk)
+            mma_bf16(d, sw128_desc(sa + kk * kUK * 2), sw128_desc(sb + kk * kUK * 2), idesc, (kb | kk) != 0);
+          mma_commit(smem_addr(empty + s));
+          ++it;
+        }
+        if (ok) mma_commit(smem_addr(tfull + buf));
+      }
+      // every MMA issued completes before the tensor memory is freed
+      mma_commit(smem_addr(done));
+      mbar_wait_bounded(done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue: warps 2..5, warp w reads TMEM lanes 32 * (w % 4) .. + 31 ----
+    const int q = warp & 3;
+    const int m = q * 32 + lane;
+    int lt = 0;
+    for (int w = blockIdx.x; w < total; w += gridDim.x, ++lt) {
+      const int buf = lt & 1;
+      const uint32_t ph = (lt >> 1) & 1;
+      int ok = 0;
+      if (lane == 0) ok = role_wait(tfull + buf, ph, abort, a.err) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const Tile t = tile_of(w, pref, offs, a);
+      const bool valid = m < t.rows;
+      __nv_bfloat16 *orow = a.out + static_cast<int64_t>(t.row0 + (valid ? m : 0)) * a.n_total + t.n0;
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBNMax;
+      if (a.swiglu) {
+        for (int c = 0; c < kBNMax / 2; c += 32) {
+          uint32_t r[64];
+          tmem_load32x2_wait(tb + c, tb + kBNMax / 2 + c, r);
+          if (valid) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g0 = __uint_as_float(r[2 * i]), g1 = __uint_as_float(r[2 * i + 1]);
+              const float u0 = __uint_as_float(r[32 + 2 * i]), u1 = __uint_as_float(r[32 + 2 * i + 1]);
+              const __nv_bfloat162 b = __floats2bfloat162_rn(g0 / (1.0f + expf(-g0)) * u0, g1 / (1.0f + expf(-g1)) * u1);
+              pk[i] = *reinterpret_cast<const uint32_t *>(&b);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+      } else {
+        for (int c = 0; c < a.b_rows; c += 32) {
+          uint32_t r[32];
+          tmem_load32_wait(tb + c, r);
+          if (valid) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+              pk[i] = *reinterpret_cast<const uint32_t *>(&b);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(tempty + buf));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// 2-D bf16 map of a row-major [rows][K] matrix, boxes of 128 rows x 64 columns, 128-byte swizzle.
+bool make_map(CUtensorMap *map, const void *base, int64_t K, int64_t rows) {
+  const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBoxRows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int gemm_smem_bytes(int E) { return kSmemFixed + 8 * (E + 1); }
+
+moe_status launch_grouped(GemmArgs a, const void *A, const void *B0, const void *B1, int64_t b_total_rows,
+                          int num_sms, cudaStream_t stream) {
+  const int smem = gemm_smem_bytes(a.E);
+  if (smem > kSmemMax) return MOE_EINVAL;
+  const int64_t max_tiles = (static_cast<int64_t>(a.rows) / kBM + a.E) * a.ntiles_n;
+  if (max_tiles > INT32_MAX) return MOE_EINVAL;
+  CUtensorMap ma, mb0, mb1;
+  if (!make_map(&ma, A, a.K, a.rows) || !make_map(&mb0, B0, a.K, b_total_rows) ||
+      !make_map(&mb1, B1, a.K, b_total_rows))
+    return MOE_ECUDA;
+  if (cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return MOE_ECUDA;
+  const int sms = num_sms > 0 ? num_sms : sm_count();
+  const int64_t grid = max_tiles < sms ? max_tiles : sms;
+  if (grid <= 0) return MOE_OK;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  use_pdl(cfg, attr);
+  if (cudaLaunchKernelEx(&cfg, grouped_gemm_kernel, ma, mb0, mb1, a) != cudaSuccess) return MOE_ECUDA;
+  return launch_status();
+}
+
+// Checks shared by both linear maps; fills rows (= R * T * k packed rows).
+moe_status check_expert(const moe_desc *desc, int32_t inter, Sizes *s, int64_t *rows) {
+  moe_status st = check_desc(desc, s);
+  if (st != MOE_OK) return st;
+  if (s->dtype != MOE_BF16) return MOE_EINVAL;
+  if (s->H % 128 != 0 || inter < 128 || inter % 128 != 0) return MOE_EINVAL;
+  if (static_cast<int64_t>(s->E) * inter > INT32_MAX || static_cast<int64_t>(s->E) * s->H > INT32_MAX)
+    return MOE_EINVAL;
+  *rows = s->ntok * s->k;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status moe_expert_gate_up(const moe_desc *desc, int32_t inter, const int32_t *region_offsets,
+                                         const void *packed_x, const void *w_gate, const void *w_up, void *h,
+                                         int32_t *err, void *stream) {
+  Sizes s;
+  int64_t rows = 0;
+  moe_status st = check_expert(desc, inter, &s, &rows);
+  if (st != MOE_OK) return st;
+  if (region_offsets == nullptr || err == nullptr || !aligned4(region_offsets) || !aligned4(err)) return MOE_EINVAL;
+  if (rows == 0) return MOE_OK;
+  if (packed_x == nullptr || w_gate == nullptr || w_up == nullptr || h == nullptr) return MOE_EINVAL;
+  if (!aligned16(packed_x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(h)) return MOE_EINVAL;
+  GemmArgs a{region_offsets, err, static_cast<__nv_bfloat16 *>(h), static_cast<int>(rows), s.E, s.R, s.H,
+             inter, kBNMax, kBNMax / 2, inter / (kBNMax / 2), inter, 1};
+  return launch_grouped(a, packed_x, w_gate, w_up, static_cast<int64_t>(s.E) * inter, desc->num_sms,
+                        static_cast<cudaStream_t>(stream));
+}
+
+extern "C" moe_status moe_expert_down(const moe_desc *desc, int32_t inter, const int32_t *region_offsets,
+                                      const void *h, const void *w_down, void *packed_y, int32_t *err,
+                                      void *stream) {
+  Sizes s;
+  int64_t rows = 0;
+  moe_status st = check_expert(desc, inter, &s, &rows);
+  if (st != MOE_OK) return st;
+  if (region_offsets == nullptr || err == nullptr || !aligned4(region_offsets) || !aligned4(err)) return MOE_EINVAL;
+  if (rows == 0) return MOE_OK;
+  if (h == nullptr || w_down == nullptr || packed_y == nullptr) return MOE_EINVAL;
+  if (!aligned16(h) || !aligned16(w_down) || !aligned16(packed_y)) return MOE_EINVAL;
+  const int bn = s.H % kBNMax == 0 ? kBNMax : kBoxRows;
+  GemmArgs a{region_offsets, err, static_cast<__nv_bfloat16 *>(packed_y), static_cast<int>(rows), s.E, s.R,
+             inter, s.H, bn, bn, s.H / bn, s.H, 0};
+  return launch_grouped(a, h, w_down, w_down, static_cast<int64_t>(s.E) * s.H, desc->num_sms,
+                        static_cast<cudaStream_t>(stream));
+}

@@ -116,5 +116,13 @@ class MoeStep:
         B.moe_combine_packed(self.desc, packed_y, packed.tok_packed, d.topk_weights, b.flags,
                              b.out if out is None else out, b.err, stream)
 
+    def expert_mlp(self, weights, packed: B.PackedBuffers, h: torch.Tensor, packed_y: torch.Tensor, stream=None):
+        """The expert stage on the packed rows: linear 1 with SwiGLU into h [R*T*k][I],
+        then linear 2 into packed_y [R*T*k][H] (what combine_packed reads)."""
+        b = self.buf
+        B.moe_expert_gate_up(self.desc, weights.inter, packed.region_offsets, packed.packed_x, weights.w_gate,
+                             weights.w_up, h, b.err, stream)
+        B.moe_expert_down(self.desc, weights.inter, packed.region_offsets, h, weights.w_down, packed_y, b.err, stream)
+
     def error(self, stream=None) -> int:
         return B.moe_get_error(self.buf.err, stream)

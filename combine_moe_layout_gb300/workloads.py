@@ -41,6 +41,7 @@ class Workload:
     expert: str             # "identity" or "scale" (y = x * (1 + e/256))
     x_dist: str             # "uniform" (U(-1,1)) or "normal" (N(0,1))
     seed: int = 0
+    intermediate: int = 0   # I of the expert MLP (linear 1: H -> 2I with SwiGLU, linear 2: I -> H)
 
     @property
     def local_experts(self) -> int:
@@ -90,15 +91,22 @@ class Workload:
                 "total": lay + dis + com, "total_packed": lay + dis + rcv + com + N * k * 4}
 
 
+# Expert MLP widths I: DeepSeek-V3 experts 2048, Mixtral 8x7B experts 14336 (the
+# models' published configurations; the pages give hidden sizes, not these).
 WORKLOADS = {
-    "tiny": Workload("tiny", 2, 16, 128, 8, 2, 16, "bf16", "softmax", True, "identity", "uniform"),
-    "ds_decode": Workload("ds_decode", 8, 128, 7168, 256, 8, 128, "fp8", "softmax", False, "scale", "normal"),
-    "mixtral": Workload("mixtral", 8, 4096, 4096, 8, 2, 4096, "bf16", "softmax", True, "identity", "normal"),
-    "skewed": Workload("skewed", 16, 256, 7168, 256, 8, 256, "bf16", "zipf", True, "identity", "normal"),
-    "ds_prefill": Workload("ds_prefill", 8, 4096, 7168, 256, 8, 4096, "fp8", "group", True, "scale", "normal"),
+    "tiny": Workload("tiny", 2, 16, 128, 8, 2, 16, "bf16", "softmax", True, "identity", "uniform",
+                     intermediate=256),
+    "ds_decode": Workload("ds_decode", 8, 128, 7168, 256, 8, 128, "fp8", "softmax", False, "scale", "normal",
+                          intermediate=2048),
+    "mixtral": Workload("mixtral", 8, 4096, 4096, 8, 2, 4096, "bf16", "softmax", True, "identity", "normal",
+                        intermediate=14336),
+    "skewed": Workload("skewed", 16, 256, 7168, 256, 8, 256, "bf16", "zipf", True, "identity", "normal",
+                       intermediate=2048),
+    "ds_prefill": Workload("ds_prefill", 8, 4096, 7168, 256, 8, 4096, "fp8", "group", True, "scale", "normal",
+                           intermediate=2048),
     # the decode shape with bf16 rows quantised to fp8 + scales on dispatch
     "ds_decode_bf16in": Workload("ds_decode_bf16in", 8, 128, 7168, 256, 8, 128, "bf16q", "softmax", False, "scale",
-                                 "normal"),
+                                 "normal", intermediate=2048),
 }
 
 DESCRIPTIONS = {
@@ -244,3 +252,29 @@ def make_inputs(w: Workload, seed: int | None = None) -> Inputs:
     else:
         x, sc = _to_bf16_bits(xf).reshape(R, T, H), None
     return Inputs(idx.reshape(R, T, k), wts.reshape(R, T, k), x, sc)
+
+
+# --- expert weights (input generation only) ----------------------------------
+
+@dataclass
+class ExpertWeights:
+    inter: int
+    w_gate: torch.Tensor  # [E][I][H] bf16
+    w_up: torch.Tensor    # [E][I][H] bf16
+    w_down: torch.Tensor  # [E][H][I] bf16
+
+
+def expert_weights(w: Workload, device="cpu", seed: int | None = None, inter: int | None = None) -> ExpertWeights:
+    """Synthetic bf16 expert weights: N(0, 1/K) entries (K the input width of
+    each linear map), drawn with torch's generator on `device` in the order
+    gate, up, down. No trained weights are involved."""
+    I = w.intermediate if inter is None else inter
+    E, H = w.num_experts, w.hidden
+    g = torch.Generator(device=device)
+    g.manual_seed((w.seed if seed is None else seed) + 7919)
+
+    def draw(shape, fan_in):
+        t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        return t.mul_(fan_in ** -0.5).to(torch.bfloat16)
+
+    return ExpertWeights(I, draw((E, I, H), H), draw((E, I, H), H), draw((E, H, I), I))

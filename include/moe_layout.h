@@ -213,6 +213,37 @@ moe_status moe_route_stats(const moe_desc *desc, const int32_t *topk_idx, int32_
 moe_status moe_expert_stub(const moe_desc *desc, const void *recv_x, const float *recv_scales,
                            const int32_t *counts, uint16_t *expert_out, int32_t *err, void *stream);
 
+/* Expert stage, linear 1 with SwiGLU ("How GPUs Talk to Each Other During LLM
+ * Inference", section 7, Mega MoE: between dispatch and combine each expert runs
+ * linear 1, SwiGLU and linear 2; Perplexity, "Dispatch": the packed rows feed a
+ * grouped GEMM). For every packed row p of expert e, i.e. region_offsets[e*R]
+ * <= p < region_offsets[(e+1)*R]:
+ *   h[p][i] = bf16_rne( silu(g) * u ),  silu(g) = g / (1 + exp(-g)),
+ *   g = sum_c x[p][c] w_gate[e][i][c],  u = sum_c x[p][c] w_up[e][i][c],
+ * bf16 products accumulated in fp32 on the tensor cores, silu in fp32.
+ *   desc: dtype MOE_BF16, hidden H a multiple of 128; inter I a multiple of 128.
+ *   region_offsets [E*R + 1] int32 (read; as moe_dispatch_recv writes them).
+ *   packed_x [R*T*k][H] bf16 (read); w_gate, w_up [E][I][H] bf16 (read);
+ *   h [R*T*k][I] bf16 (written for packed rows only). All four 16-byte aligned.
+ * Host errors: MOE_EINVAL for another dtype, sizes or alignment, or more experts
+ * than fit in shared memory (about 3900); MOE_ECUDA when no TMA tensor map can
+ * be made. Device errors: an expert whose offsets are not a range inside
+ * [0, R*T*k] -> MOE_EINVAL (its rows are skipped); a stalled pipeline ->
+ * MOE_ETIMEOUT. */
+moe_status moe_expert_gate_up(const moe_desc *desc, int32_t inter, const int32_t *region_offsets,
+                              const void *packed_x, const void *w_gate, const void *w_up, void *h, int32_t *err,
+                              void *stream);
+
+/* Expert stage, linear 2 (same passages): for every packed row p of expert e,
+ *   packed_y[p][j] = bf16_rne( sum_i h[p][i] w_down[e][j][i] ),
+ * fp32 accumulation on the tensor cores. packed_y is what moe_combine_packed
+ * reads.
+ *   h [R*T*k][I] bf16 (read); w_down [E][H][I] bf16 (read); packed_y [R*T*k][H]
+ *   bf16 (written for packed rows only). Sizes, alignment and errors as
+ *   moe_expert_gate_up. */
+moe_status moe_expert_down(const moe_desc *desc, int32_t inter, const int32_t *region_offsets, const void *h,
+                           const void *w_down, void *packed_y, int32_t *err, void *stream);
+
 /* Combine (Perplexity, "Combine"; "How GPUs Talk", section 7). For every token:
  * out[src][t][h] = bf16_rne( sum_{j<k} w[src][t][j] * Y[tok_slot[src][t][j]][h] ),
  * the products and sum in fp32, choices in order j = 0..k-1, weights applied at
