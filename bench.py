@@ -432,6 +432,229 @@ def run_native(args, rank, local_rank, world):
     return line
 
 
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s from MEASURED_PEAKS.json: (burst, sustained, kind)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["bf16_tflops"]), float(m["bf16_tflops_sustained"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, "fallback"
+
+
+def run_expert(args, rank, local_rank, world):
+    """One step = fused layout+dispatch -> receive hook -> expert stage (linear 1 +
+    SwiGLU, linear 2 on the tensor cores) -> packed combine, on a bf16 workload
+    with synthetic expert weights resident in HBM."""
+    import numpy as np
+    import torch
+
+    from combine_moe_layout_gb300 import _binding as B
+    from combine_moe_layout_gb300 import pipeline as P
+    from combine_moe_layout_gb300 import workloads as wl
+
+    assert torch.cuda.is_available(), "the native arm needs a CUDA device"
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    init_dist(world, "nccl")
+    w = wl.WORKLOADS[args.workload]
+    if args.tokens_per_rank or args.intermediate:
+        from dataclasses import replace
+        T_ = args.tokens_per_rank or w.tokens_per_rank
+        I_ = args.intermediate or w.intermediate
+        w = replace(w, name=f"{w.name}_T{T_}_I{I_}", tokens_per_rank=T_, max_m=T_, intermediate=I_)
+        wl.DESCRIPTIONS.setdefault(w.name, f"{wl.DESCRIPTIONS[args.workload]}; {T_} tokens per rank, I {I_}")
+    if w.dtype != "bf16":
+        raise SystemExit(f"--expert needs a bf16 workload, {w.name} is {w.dtype}")
+    inp = wl.make_inputs(w)
+    step = P.MoeStep(w, dev, args.num_sms)
+    d = P.to_device(inp, dev)
+    wts = wl.expert_weights(w, dev)
+    packed = B.allocate_packed(step.desc, dev)
+    rows, H, I = w.num_tokens * w.topk, w.hidden, w.intermediate
+    h = torch.empty((rows, I), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    step.reset()
+
+    stages = [("layout_dispatch", lambda dd, out=None: step.layout_dispatch(dd)),
+              ("recv", lambda dd, out=None: step.recv(packed)),
+              ("expert_gate_up", lambda dd, out=None: B.moe_expert_gate_up(
+                  step.desc, I, packed.region_offsets, packed.packed_x, wts.w_gate, wts.w_up, h, step.buf.err)),
+              ("expert_down", lambda dd, out=None: B.moe_expert_down(
+                  step.desc, I, packed.region_offsets, h, wts.w_down, y, step.buf.err)),
+              ("combine_packed", lambda dd, out=None: step.combine_packed(dd, y, packed, out=out))]
+
+    def path(dd, out=None):
+        for _, fn in stages:
+            fn(dd, out)
+
+    path(d)
+    if step.error() != B.MOE_OK:
+        raise RuntimeError("first expert step failed")
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(flush_w.numel() // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_w.fill_(1)
+        flush_r.sum()
+
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        flush()
+        path(d)
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler = ClockSampler(local_rank).start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush()
+        ev[i][0].record(stream)
+        path(d)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
+    for i in range(K):
+        flush()
+        kev[i][0].record(stream)
+        for j, (_, fn) in enumerate(stages):
+            fn(d)
+            kev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    kern_ms = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in kev) for j, (name, _) in enumerate(stages)}
+
+    # end to end: routing, rows and weights read from pinned host memory and the
+    # bf16 output written there by the kernels themselves (zero-copy over NVLink-C2C)
+    e2e = None
+    if not args.no_e2e:
+        hd = P.to_pinned_host(inp)
+        hout = torch.empty((w.num_ranks, w.tokens_per_rank, H), dtype=torch.bfloat16).pin_memory()
+        eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            flush()
+            eev[i][0].record(stream)
+            path(hd, out=hout)
+            eev[i][1].record(stream)
+        torch.cuda.synchronize()
+        nbytes = inp.x.nbytes + inp.topk_idx.nbytes + inp.topk_weights.nbytes
+        e2e = {"value": None, "unit": "tokens/s", "h2d_bytes_per_step": int(nbytes),
+               "d2h_bytes_per_step": hout.numel() * 2,
+               "local_ms_total": sum(a.elapsed_time(b) for a, b in eev),
+               "copies": "zero-copy: the kernels read routing and rows from pinned host memory and write the "
+                         "bf16 output into pinned host memory over NVLink-C2C"}
+        path(d)
+        torch.cuda.synchronize()
+        if not torch.equal(hout.view(torch.int16), step.buf.out.cpu().view(torch.int16)):
+            raise RuntimeError("end-to-end output differs from the device output")
+    clocks = sampler.stop()
+    if step.error() != B.MOE_OK:
+        raise RuntimeError("timed expert steps latched an error")
+    job = whole_job(w.num_tokens, sum(step_ms), K, world, dev)
+    if e2e is not None:
+        ej = whole_job(w.num_tokens, e2e.pop("local_ms_total"), K, world, dev)
+        e2e["value"], e2e["ms_per_step"] = ej["value"], ej["ms_per_step"]
+    if rank != 0:
+        return None
+
+    flops = {"expert_gate_up": 2 * rows * H * 2 * I, "expert_down": 2 * rows * I * H}
+    # bytes each linear map must move at least once: the weights of the experts
+    # that received rows, the packed input rows, the output rows
+    used = int((packed.region_offsets[w.num_ranks::w.num_ranks].cpu() -
+                packed.region_offsets[:-1:w.num_ranks].cpu() > 0).sum())
+    gbytes = {"expert_gate_up": used * 2 * I * H * 2 + rows * H * 2 + rows * I * 2,
+              "expert_down": used * H * I * 2 + rows * I * 2 + rows * H * 2}
+    weight_bytes = 3 * w.num_experts * I * H * 2
+    burst, sustained, kind = measured_tensor_peak()
+    hbm, hbm_kind = measured_hbm_peak()
+    top = max(flops, key=lambda n: kern_ms[n])
+    # the kernel's bound: whichever of its flops and its bytes takes longer at the measured peaks
+    tensor_bound = flops[top] / (sustained * 1e12) >= gbytes[top] / (hbm * 1e9)
+    ab = dict(w.algorithmic_bytes())
+    kernel_stats = {}
+    for name, ms in kern_ms.items():
+        st = {"us": round(ms * 1e3, 3)}
+        if name in flops:
+            tf = flops[name] / (ms / 1e3) / 1e12
+            gbs = gbytes[name] / (ms / 1e3) / 1e9
+            st.update({"flops": flops[name], "TFLOPs": round(tf, 1), "frac_of_sustained_bf16": round(tf / sustained, 4),
+                       "frac_of_burst_bf16": round(tf / burst, 4), "algorithmic_bytes": gbytes[name],
+                       "GBps": round(gbs, 1), "frac_of_measured_hbm": round(gbs / hbm, 4)})
+        else:
+            key = {"layout_dispatch": None, "recv": "recv", "combine_packed": "combine_packed"}[name]
+            nbytes = ab["layout"] + ab["dispatch"] if key is None else ab[key]
+            st.update({"algorithmic_bytes": nbytes, "GBps": round(nbytes / (ms / 1e3) / 1e9, 1)})
+        kernel_stats[name] = st
+    line = {
+        "metric": METRIC, "value": round(job["value"], 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(job["ms_per_step"], 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "impl": "native",
+        "config": {
+            "workload": w.name + "+experts", "description": wl.DESCRIPTIONS[w.name],
+            "expert_mlp": f"{w.num_experts} experts, linear 1 {H}->2x{I} with SwiGLU, linear 2 {I}->{H}, bf16 "
+                          f"weights N(0,1/K) ({weight_bytes / 1e9:.2f} GB resident)",
+            "tokens_per_step_per_gpu": w.num_tokens, "flops_per_step": sum(flops.values()),
+            "path": "fused layout+dispatch -> receive hook (expert-major packing) -> linear 1 + SwiGLU -> linear 2 "
+                    "(tcgen05 grouped GEMMs, fp32 accumulate) -> packed combine",
+            "l2": "flushed before every timed step, outside the timed events",
+            "launch": "direct launches through the C ABI",
+            "parallelism": "replicas only: one independent EP group per GPU",
+        },
+        "roofline": ({"kernel": "grouped_gemm_kernel (" + top + ")", "bound": "tensor",
+                      "achieved": kernel_stats[top]["TFLOPs"], "peak": sustained,
+                      "peak_kind": f"{kind} bf16 dense, sustained (the kernel runs inside a multi-ms step)",
+                      "unit": "TFLOP/s", "frac": kernel_stats[top]["frac_of_sustained_bf16"],
+                      "frac_of_burst": kernel_stats[top]["frac_of_burst_bf16"],
+                      "traffic": profiled_traffic("moe_expert.cu", w.name),
+                      "algorithmic_flops_per_launch": flops[top]} if tensor_bound else
+                     {"kernel": "grouped_gemm_kernel (" + top + ")", "bound": "hbm",
+                      "achieved": kernel_stats[top]["GBps"], "peak": hbm, "peak_kind": f"{hbm_kind} (copy bandwidth)",
+                      "unit": "GB/s", "frac": kernel_stats[top]["frac_of_measured_hbm"],
+                      "traffic": profiled_traffic("moe_expert.cu", w.name),
+                      "algorithmic_bytes_per_launch": gbytes[top]}),
+        "kernels": kernel_stats,
+        "kernel_timing": "CUDA events between the launches, a second pass of the same K steps",
+        "e2e": e2e, "gpu_launches": (B.moe_layout_dispatch_kernels(step.desc) + 5) * K,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_expert(w, inp, args.cpu_seconds)
+    return line
+
+
+def cpu_baseline_expert(w, inp, seconds: float) -> dict:
+    """The oracle's layout over all tokens plus the expert MLP of the k choices of
+    sampled tokens (about `seconds` of CPU work), as tokens/s."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from combine_moe_layout_gb300 import workloads as wl
+    t0 = time.perf_counter()
+    oracle.layout(inp.topk_idx, w.num_experts, w.max_m)
+    t_layout = time.perf_counter() - t0
+    wts = wl.expert_weights(w, "cpu")
+    bits = [t.view(torch.int16).numpy().view(np.uint16) for t in (wts.w_gate, wts.w_up, wts.w_down)]
+    x = inp.x.reshape(w.num_tokens, w.hidden)
+    idx = inp.topk_idx.reshape(w.num_tokens, w.topk)
+    spent, n = 0.0, 0
+    while n < 1 or spent < seconds:
+        tok = (n * 7919) % w.num_tokens
+        t0 = time.perf_counter()
+        for e in idx[tok]:
+            oracle.expert_mlp_row(x[tok], bits[0][e], bits[1][e], bits[2][e])
+        spent += time.perf_counter() - t0
+        n += 1
+    per_tok = spent / n + t_layout / w.num_tokens
+    return {"value": round(1.0 / per_tok, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"layout of all {w.num_tokens} tokens + the {w.topk} expert MLP rows of {n} tokens, "
+                      f"single-threaded C oracle (fp64)", "seconds": round(spent + t_layout, 2),
+            "cpu": _cpu_model()}
+
+
 # --- the CPU oracle (baseline leg and reference arm) ---------------------------------
 
 def _oracle_sample_step(w, inp, sel):
@@ -576,6 +799,11 @@ def main(argv=None):
     ap.add_argument("--graph", action="store_true", help="replay the step's launches from a CUDA graph")
     ap.add_argument("--packed", action="store_true",
                     help="step = layout+dispatch, the receive hook (expert-major packing), the packed combine")
+    ap.add_argument("--expert", action="store_true",
+                    help="step = layout+dispatch, receive hook, expert stage (linear 1 + SwiGLU, linear 2 on the "
+                         "tensor cores), packed combine; bf16 workload (default mixtral)")
+    ap.add_argument("--tokens-per-rank", type=int, default=0, help="--expert: override T (a smaller profiling case)")
+    ap.add_argument("--intermediate", type=int, default=0, help="--expert: override the expert MLP width I")
     ap.add_argument("--calibrate", action="store_true",
                     help="print the bandwidth of plain device writes and copies at the step's sizes and exit")
     ap.add_argument("--no-e2e", action="store_true")
@@ -584,10 +812,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)
+    if args.expert and args.workload == DEFAULT_WORKLOAD:
+        args.workload = "mixtral"
     if args.steps is None:
-        args.steps = 2000 if args.impl == "native" else 20
+        args.steps = (50 if args.expert else 2000) if args.impl == "native" else 20
     if args.warmup is None:
-        args.warmup = 20 if args.impl == "native" else 3
+        args.warmup = (5 if args.expert else 20) if args.impl == "native" else 3
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
     rank, local_rank, world = dist_env()
@@ -596,7 +826,8 @@ def main(argv=None):
     if args.calibrate:
         print(json.dumps(calibrate(local_rank)), flush=True)
         return
-    line = (run_native if args.impl == "native" else run_reference)(args, rank, local_rank, world)
+    native = run_expert if args.expert else run_native
+    line = (native if args.impl == "native" else run_reference)(args, rank, local_rank, world)
     if line is not None and rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -57,9 +57,13 @@ def library_path() -> str:
 def load():
     """Build (if stale) and open libmoe_layout.so; raises if that is impossible."""
     global _lib
-    if _lib is not None:
-        return _lib
-    path = _build.build()
+    if _lib is None:
+        _lib = _open(_build.build())
+    return _lib
+
+
+def _open(path: str):
+    """Open a build of the library at `path` and declare its entry points."""
     lib = ctypes.CDLL(path)
     vp, st = ctypes.c_void_p, ctypes.c_int32
     pdesc = ctypes.POINTER(MoeDesc)
@@ -85,7 +89,6 @@ def load():
                  "moe_expert_gate_up", "moe_expert_down",
                  "moe_get_error"):
         getattr(lib, name).restype = st
-    _lib = lib
     return lib
 
 

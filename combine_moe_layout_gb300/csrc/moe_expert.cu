@@ -29,9 +29,11 @@
 // A tile is up to 128 consecutive packed rows of one expert. For gate/up its
 // 256 accumulator columns are 128 gate rows i0..i0+127 of the expert's weights
 // followed by the 128 up rows of the same i, so SwiGLU pairs columns c and
-// c + 128 of a thread's own row. Tiles are numbered expert by expert, n-tile by
-// n-tile, with the m-tiles innermost: CTAs that run at the same time share one
-// expert's weight tile through L2.
+// c + 128 of a thread's own row. Tiles are numbered expert by expert; inside an
+// expert, in groups of G n-tiles, each group swept m-tile by m-tile with its G
+// n-tiles innermost. The CTAs running at one time then share both the group's
+// weight tiles (G of them, sized to stay in L2 for the whole sweep) and each
+// m-tile of rows (read once per group instead of once per n-tile).
 //
 // Every wait is bounded: a timeout records MOE_ETIMEOUT, every role of the CTA
 // stops, the loads and MMAs already issued are waited for (again bounded) and
@@ -60,6 +62,11 @@ constexpr int kGemmThreads = 192;
 constexpr uint32_t kTmemCols = 2 * kBNMax;
 constexpr int kSmemFixed = 1024 + kStages * kStage + (2 * kStages + 5) * 8 + 8;
 constexpr int kSmemMax = 227 * 1024;
+// L2 bytes the weight tiles of one n-tile group may take (the group's G tiles
+// stay resident while the group sweeps the expert's rows)
+#ifndef MOE_GEMM_L2_GROUP_BYTES
+#define MOE_GEMM_L2_GROUP_BYTES (48ll << 20)
+#endif
 
 // tcgen05 shared-memory matrix descriptor of a K-major bf16 tile as TMA writes
 // it with the 128-byte swizzle: 128-byte rows (64 elements), 8-row groups 1024
@@ -192,14 +199,16 @@ struct GemmArgs {
   int ntiles_n;                   // n_total / out_cols
   int expert_rows;                // weight rows of one expert in the tensor maps (I or H)
   int swiglu;                     // 1: gate/up tile with the SwiGLU epilogue
+  int group_n;                    // n-tiles per group of the tile order (>= 1)
 };
 
 struct Tile {
   int e, row0, rows, n0;
 };
 
-// Tile w of the CTA's sequence: its expert (pref[e] <= w < pref[e + 1]), then
-// n-tile and m-tile with the m-tiles innermost.
+// Tile w of the CTA's sequence: its expert (pref[e] <= w < pref[e + 1]), its
+// group of group_n n-tiles (the last group may be narrower), then m-tile and,
+// innermost, the n-tile within the group.
 __device__ __forceinline__ Tile tile_of(int w, const int32_t *pref, const int32_t *offs, const GemmArgs &a) {
   int lo = 0, hi = a.E - 1;
   while (lo < hi) {
@@ -214,7 +223,10 @@ __device__ __forceinline__ Tile tile_of(int w, const int32_t *pref, const int32_
   const int m = offs[lo + 1] - offs[lo];
   const int mtiles = (m + kBM - 1) / kBM;
   const int local = w - pref[lo];
-  const int nt = local / mtiles, mt = local - nt * mtiles;
+  const int per_group = mtiles * a.group_n;
+  const int g = local / per_group, r = local - g * per_group;
+  const int gw = min(a.group_n, a.ntiles_n - g * a.group_n);
+  const int mt = r / gw, nt = g * a.group_n + (r - mt * gw);
   t.row0 = offs[lo] + mt * kBM;
   t.rows = min(kBM, m - mt * kBM);
   t.n0 = nt * a.out_cols;
@@ -465,6 +477,8 @@ int gemm_smem_bytes(int E) { return kSmemFixed + 8 * (E + 1); }
 
 moe_status launch_grouped(GemmArgs a, const void *A, const void *B0, const void *B1, int64_t b_total_rows,
                           int num_sms, cudaStream_t stream) {
+  const int64_t group = MOE_GEMM_L2_GROUP_BYTES / (static_cast<int64_t>(a.b_rows) * a.K * 2);
+  a.group_n = static_cast<int>(group < 1 ? 1 : (group > a.ntiles_n ? a.ntiles_n : group));
   const int smem = gemm_smem_bytes(a.E);
   if (smem > kSmemMax) return MOE_EINVAL;
   const int64_t max_tiles = (static_cast<int64_t>(a.rows) / kBM + a.E) * a.ntiles_n;
@@ -518,7 +532,7 @@ extern "C" moe_status moe_expert_gate_up(const moe_desc *desc, int32_t inter, co
   if (packed_x == nullptr || w_gate == nullptr || w_up == nullptr || h == nullptr) return MOE_EINVAL;
   if (!aligned16(packed_x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(h)) return MOE_EINVAL;
   GemmArgs a{region_offsets, err, static_cast<__nv_bfloat16 *>(h), static_cast<int>(rows), s.E, s.R, s.H,
-             inter, kBNMax, kBNMax / 2, inter / (kBNMax / 2), inter, 1};
+             inter, kBNMax, kBNMax / 2, inter / (kBNMax / 2), inter, 1, 1};
   return launch_grouped(a, packed_x, w_gate, w_up, static_cast<int64_t>(s.E) * inter, desc->num_sms,
                         static_cast<cudaStream_t>(stream));
 }
@@ -536,7 +550,7 @@ extern "C" moe_status moe_expert_down(const moe_desc *desc, int32_t inter, const
   if (!aligned16(h) || !aligned16(w_down) || !aligned16(packed_y)) return MOE_EINVAL;
   const int bn = s.H % kBNMax == 0 ? kBNMax : kBoxRows;
   GemmArgs a{region_offsets, err, static_cast<__nv_bfloat16 *>(packed_y), static_cast<int>(rows), s.E, s.R,
-             inter, s.H, bn, bn, s.H / bn, s.H, 0};
+             inter, s.H, bn, bn, s.H / bn, s.H, 0, 1};
   return launch_grouped(a, h, w_down, w_down, static_cast<int64_t>(s.E) * s.H, desc->num_sms,
                         static_cast<cudaStream_t>(stream));
 }

@@ -216,6 +216,25 @@ def test_expert_stage_feeds_the_packed_combine():
     free_gpu()
 
 
+def test_expert_stage_with_narrow_tile_groups():
+    """A build whose L2 budget per n-tile group is 256 KiB: groups of two gate/up
+    n-tiles out of three (a narrower last group) and single-tile groups, the
+    same results within the same bars."""
+    require_gpu()
+    import os
+
+    from combine_moe_layout_gb300 import _build
+    path = os.path.join(os.path.dirname(_build.LIB), "libmoe_layout_group256k.so")
+    variant = B._open(_build.build(extra_flags=["-DMOE_GEMM_L2_GROUP_BYTES=262144"], lib_path=path))
+    real = B.load()
+    try:
+        B._lib = variant
+        for name in ("ragged", "zipf"):
+            test_expert_stage_matches_oracle(name)
+    finally:
+        B._lib = real
+
+
 def test_expert_stage_rejects_what_it_cannot_run():
     require_gpu()
     w = CASES["tiny"]
