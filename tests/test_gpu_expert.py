@@ -41,6 +41,10 @@ CASES = {
     # Zipf routing: hot experts with many tiles, empty experts; H = 384 gives three 128-wide down tiles
     "zipf": wl.custom("expert_zipf", num_ranks=4, tokens_per_rank=256, hidden=384, num_experts=32, topk=4,
                       max_m=256, router="zipf", x_dist="normal", intermediate=256),
+    # 1200 rows per expert on average: the default build takes the CTA-pair kernel
+    # (five 256-row pair tiles per expert, the last one ragged)
+    "pair_default": wl.custom("expert_pair", num_ranks=4, tokens_per_rank=600, hidden=256, num_experts=4, topk=2,
+                              max_m=600, x_dist="normal", intermediate=256),
 }
 
 
@@ -235,6 +239,36 @@ def test_expert_stage_with_narrow_tile_groups():
         B._lib = real
 
 
+def _with_variant(flags, name, cases):
+    import os
+
+    from combine_moe_layout_gb300 import _build
+    path = os.path.join(os.path.dirname(_build.LIB), name)
+    variant = B._open(_build.build(extra_flags=flags, lib_path=path))
+    real = B.load()
+    try:
+        B._lib = variant
+        for c in cases:
+            test_expert_stage_matches_oracle(c)
+    finally:
+        B._lib = real
+
+
+def test_expert_stage_pair_kernel_single_accumulator():
+    """The CTA-pair kernel forced on (the default build takes it only for experts
+    of 512 rows or more on average, as in the Mixtral-shape test), with one
+    256-column accumulator per CTA: the same results within the same bars."""
+    require_gpu()
+    _with_variant(["-DMOE_GEMM_PAIR=2", "-DMOE_GEMM_PAIR_TMEM_COLS=256"], "libmoe_layout_pair256.so",
+                  ("ragged", "tiny", "zipf"))
+
+
+def test_expert_stage_pair_kernel_double_accumulator():
+    """The CTA-pair kernel forced on, with two 256-column accumulators per CTA."""
+    require_gpu()
+    _with_variant(["-DMOE_GEMM_PAIR=2"], "libmoe_layout_pair512.so", ("ragged", "tiny", "zipf"))
+
+
 def test_expert_stage_rejects_what_it_cannot_run():
     require_gpu()
     w = CASES["tiny"]
@@ -257,8 +291,8 @@ def test_expert_stage_rejects_what_it_cannot_run():
 
 def test_expert_stage_on_the_mixtral_shape_sampled_rows():
     """The full Mixtral 8x7B expert shape (H 4096, I 14336, 8 experts, 65536
-    packed rows), checked on sampled rows of two experts: the first and last
-    row of each expert's range and rows in between."""
+    packed rows; the CTA-pair kernel), checked on sampled rows of two experts:
+    the first and last row of each expert's range and rows in between."""
     require_gpu()
     w = wl.WORKLOADS["mixtral"]
     inp = wl.make_inputs(w)
