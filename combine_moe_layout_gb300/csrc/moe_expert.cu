@@ -18,8 +18,8 @@
 //
 // Two kernels share the scheme below: grouped_gemm_kernel (one CTA per tile,
 // M = 128) and grouped_gemm_pair_kernel (a cluster of two CTAs per tile,
-// M = 256 with tcgen05 cta_group::2), taken for experts that average at least
-// 512 rows.
+// M = 256 with tcgen05 cta_group::2), taken for linear 2 of experts that
+// average at least 512 rows.
 //
 // Kernel shape: one persistent CTA per SM, 192 threads.
 //   warp 0      TMA producer: per 64-wide K block, a 128-row A tile and a
@@ -37,8 +37,8 @@
 // c + 128 of a thread's own row. Tiles are numbered expert by expert; inside an
 // expert, in groups of G n-tiles, each group swept m-tile by m-tile with its G
 // n-tiles innermost. The CTAs running at one time then share both the group's
-// weight tiles (G of them, sized to stay in L2 for the whole sweep) and each
-// m-tile of rows (read once per group instead of once per n-tile).
+// weight tiles and each m-tile of rows (read once per group instead of once per
+// n-tile); G balances the two (see group_width).
 //
 // Every wait is bounded: a timeout records MOE_ETIMEOUT, every role of the CTA
 // stops, the loads and MMAs already issued are waited for (again bounded) and
@@ -46,6 +46,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+
+#include <cmath>
 
 
 #include "moe_common.cuh"
@@ -67,10 +69,16 @@ constexpr int kGemmThreads = 192;
 constexpr uint32_t kTmemCols = 2 * kBNMax;
 constexpr int kSmemFixed = 1024 + kStages * kStage + (2 * kStages + 5) * 8 + 8;
 constexpr int kSmemMax = 227 * 1024;
-// L2 bytes the weight tiles of one n-tile group may take (the group's G tiles
-// stay resident while the group sweeps the expert's rows)
+// Width G of an n-tile group. The C tiles that run at one time cover about C/G
+// m-tiles of rows (a bytes each) and G weight tiles (b bytes each); the bytes
+// they touch, (C/G) a + G b, are least at G = sqrt(C a / b), capped so that the
+// group's weight tiles stay well inside L2 while the group sweeps the rows.
+// MOE_GEMM_GROUP_N > 0 fixes G instead.
+#ifndef MOE_GEMM_GROUP_N
+#define MOE_GEMM_GROUP_N 0
+#endif
 #ifndef MOE_GEMM_L2_GROUP_BYTES
-#define MOE_GEMM_L2_GROUP_BYTES (48ll << 20)
+#define MOE_GEMM_L2_GROUP_BYTES (64ll << 20)
 #endif
 
 // tcgen05 shared-memory matrix descriptor of a K-major bf16 tile as TMA writes
@@ -271,6 +279,16 @@ __device__ __forceinline__ void tile_prefix(const int32_t *offs, int32_t *pref, 
 // bf16 epilogue of one 32-column chunk of a thread's accumulator row: SwiGLU
 // over gate columns g[0..31] and up columns u[0..31], or plain rounding of
 // r[0..31]; 64 bytes stored at dst.
+#ifndef MOE_GEMM_CS_STORE
+#define MOE_GEMM_CS_STORE 0
+#endif
+__device__ __forceinline__ void store16(uint4 *d, uint4 v) {
+  if (MOE_GEMM_CS_STORE)
+    __stcs(d, v);
+  else
+    *d = v;
+}
+
 __device__ __forceinline__ void store_swiglu32(__nv_bfloat16 *dst, const uint32_t (&r)[64]) {
   uint32_t pk[16];
 #pragma unroll
@@ -282,7 +300,7 @@ __device__ __forceinline__ void store_swiglu32(__nv_bfloat16 *dst, const uint32_
   }
   uint4 *d = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-  for (int v = 0; v < 4; ++v) d[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+  for (int v = 0; v < 4; ++v) store16(d + v, make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]));
 }
 
 __device__ __forceinline__ void store_plain32(__nv_bfloat16 *dst, const uint32_t (&r)[32]) {
@@ -294,7 +312,7 @@ __device__ __forceinline__ void store_plain32(__nv_bfloat16 *dst, const uint32_t
   }
   uint4 *d = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-  for (int v = 0; v < 4; ++v) d[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+  for (int v = 0; v < 4; ++v) store16(d + v, make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]));
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -518,6 +536,35 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// L2 policies for TMA loads: weight tiles are kept (evict_last) while a group
+// of n-tiles sweeps the expert's rows; the rows themselves are streamed.
+#ifndef MOE_GEMM_HINT_B
+#define MOE_GEMM_HINT_B 0
+#endif
+#ifndef MOE_GEMM_HINT_A
+#define MOE_GEMM_HINT_A 0
+#endif
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                                      uint32_t bar_cluster, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
+      : "memory");
+}
+
 // TMA tile load into this CTA's shared memory, completing on an mbarrier that may
 // live in the peer CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y,
@@ -688,8 +735,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           const uint32_t sa = smem_addr(smem + s * kPairStage), fb = map_rank(smem_addr(full + s), 0);
           if (leader) mbar_arrive_expect_tx(full + s, 2 * kPairStage);
-          tma_load_2d_pair(sa, &map_a, kb * kBK, arow, fb);
-          tma_load_2d_pair(sa + kTileA, mb, kb * kBK, brow, fb);
+          if (MOE_GEMM_HINT_A)
+            tma_load_2d_pair_hint(sa, &map_a, kb * kBK, arow, fb, policy_evict_first());
+          else
+            tma_load_2d_pair(sa, &map_a, kb * kBK, arow, fb);
+          if (MOE_GEMM_HINT_B)
+            tma_load_2d_pair_hint(sa + kTileA, mb, kb * kBK, brow, fb, policy_evict_last());
+          else
+            tma_load_2d_pair(sa + kTileA, mb, kb * kBK, brow, fb);
           ++it;
         }
       }
@@ -827,15 +880,19 @@ int pair_smem_bytes(int E) { return kPairSmemFixed + 8 * (E + 1); }
 // Whether a launch takes the CTA-pair kernel. It needs 256-row B tiles, and it
 // pays only for experts with many rows: its 256-row tiles waste half their
 // loads and MMAs on an expert of at most 128 rows, where the weights bound the
-// kernel anyway. MOE_GEMM_PAIR: 0 never, 1 when the expected rows per expert
-// (R*T*k / E) reach kPairMinRows, 2 always (tests).
+// kernel anyway. Measured on the Mixtral shape under the GPU's power cap, it
+// wins for linear 2 (1.58 against 1.51 PFLOP/s) and loses for linear 1 with
+// SwiGLU (1.54 against 1.62: it reads three times the DRAM bytes of the
+// single-CTA kernel there), so it is taken for linear 2 only.
+// MOE_GEMM_PAIR: 0 never, 1 as above (expected rows per expert R*T*k / E of at
+// least kPairMinRows), 2 for every launch with 256-row B tiles (tests).
 #ifndef MOE_GEMM_PAIR
 #define MOE_GEMM_PAIR 1
 #endif
 constexpr int kPairMinRows = 512;
 bool use_pair(const GemmArgs &a) {
   if (MOE_GEMM_PAIR == 0 || a.b_rows != kBNMax) return false;
-  return MOE_GEMM_PAIR == 2 || a.rows / a.E >= kPairMinRows;
+  return MOE_GEMM_PAIR == 2 || (!a.swiglu && a.rows / a.E >= kPairMinRows);
 }
 
 moe_status launch_pair(const GemmArgs &a, const CUtensorMap &ma, const CUtensorMap &mb0, const CUtensorMap &mb1,
@@ -873,10 +930,20 @@ moe_status launch_pair(const GemmArgs &a, const CUtensorMap &ma, const CUtensorM
   return launch_status();
 }
 
+int group_width(const GemmArgs &a, int concurrent, int tile_rows) {
+  int64_t g = MOE_GEMM_GROUP_N;
+  if (g <= 0) {
+    g = std::llround(std::sqrt(static_cast<double>(concurrent) * tile_rows / a.b_rows));
+    const int64_t cap = MOE_GEMM_L2_GROUP_BYTES / (static_cast<int64_t>(a.b_rows) * a.K * 2);
+    if (g > cap) g = cap;
+  }
+  return static_cast<int>(g < 1 ? 1 : (g > a.ntiles_n ? a.ntiles_n : g));
+}
+
 moe_status launch_grouped(GemmArgs a, const void *A, const void *B0, const void *B1, int64_t b_total_rows,
                           int num_sms, cudaStream_t stream) {
-  const int64_t group = MOE_GEMM_L2_GROUP_BYTES / (static_cast<int64_t>(a.b_rows) * a.K * 2);
-  a.group_n = static_cast<int>(group < 1 ? 1 : (group > a.ntiles_n ? a.ntiles_n : group));
+  const int sms_all = num_sms > 0 ? num_sms : sm_count();
+  a.group_n = use_pair(a) ? group_width(a, sms_all / 2, 2 * kBM) : group_width(a, sms_all, kBM);
   const int smem = gemm_smem_bytes(a.E);
   if (smem > kSmemMax) return MOE_EINVAL;
   const int64_t max_tiles = (static_cast<int64_t>(a.rows) / kBM + a.E) * a.ntiles_n;
