@@ -1,0 +1,53 @@
+// The expert stage (linear 1 with SwiGLU, then linear 2) as one call that
+// allocates nothing: the intermediate h lives in a file-scope device array of
+// fixed size instead of a caller buffer. The pages have no counterpart of this
+// call; it serves callers that may not allocate device memory (for example
+// inside a region captured into a CUDA graph with a fixed memory plan).
+//
+// The scratch is shared by every call on a device: two calls whose work
+// overlaps in time (different streams, or graphs replayed concurrently) race on
+// it. Rows of the scratch that a call does not write are read only into output
+// rows that are never stored (rows past an expert's end), so it is not cleared.
+#include <mutex>
+
+#include "moe_common.cuh"
+
+namespace {
+
+constexpr size_t kScratchBytes = size_t(32) << 20;  // h of at most R*T*k x I bf16 = 32 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_expert_h_scratch[kScratchBytes];
+
+// Device address of the scratch on the current device, looked up once per device.
+void *scratch_address() {
+  static std::mutex mu;
+  static void *addr[kMaxDevices] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_expert_h_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" moe_status moe_expert_mlp_noalloc(const moe_desc *desc, int32_t inter, const int32_t *region_offsets,
+                                             const void *packed_x, const void *w_gate, const void *w_up,
+                                             const void *w_down, void *packed_y, int32_t *err, void *stream) {
+  moe::Sizes s;
+  const moe_status st = moe::check_desc(desc, &s);
+  if (st != MOE_OK) return st;
+  if (inter < 1) return MOE_EINVAL;
+  const int64_t rows = s.ntok * s.k;
+  if (static_cast<uint64_t>(rows) * static_cast<uint64_t>(inter) * 2u > kScratchBytes) return MOE_ENOMEM;
+  void *h = scratch_address();
+  if (h == nullptr) return MOE_ECUDA;
+  const moe_status a = moe_expert_gate_up(desc, inter, region_offsets, packed_x, w_gate, w_up, h, err, stream);
+  if (a != MOE_OK) return a;
+  return moe_expert_down(desc, inter, region_offsets, h, w_down, packed_y, err, stream);
+}

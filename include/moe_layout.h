@@ -244,6 +244,18 @@ moe_status moe_expert_gate_up(const moe_desc *desc, int32_t inter, const int32_t
 moe_status moe_expert_down(const moe_desc *desc, int32_t inter, const int32_t *region_offsets, const void *h,
                            const void *w_down, void *packed_y, int32_t *err, void *stream);
 
+/* The expert stage (moe_expert_gate_up then moe_expert_down) in one call that
+ * allocates nothing. The pages have no counterpart of this call: it exists for
+ * callers that may not allocate device memory. h is kept in a fixed device array
+ * of the library (32 MiB), so R*T*k * inter * 2 bytes may not exceed 32 MiB
+ * (MOE_ENOMEM otherwise, nothing launched). The array is shared by all calls on
+ * a device: calls whose work overlaps in time race on it. Arguments, results
+ * and other errors as moe_expert_gate_up and moe_expert_down; MOE_ECUDA if the
+ * array's address cannot be obtained. */
+moe_status moe_expert_mlp_noalloc(const moe_desc *desc, int32_t inter, const int32_t *region_offsets,
+                                  const void *packed_x, const void *w_gate, const void *w_up, const void *w_down,
+                                  void *packed_y, int32_t *err, void *stream);
+
 /* Combine (Perplexity, "Combine"; "How GPUs Talk", section 7). For every token:
  * out[src][t][h] = bf16_rne( sum_{j<k} w[src][t][j] * Y[tok_slot[src][t][j]][h] ),
  * the products and sum in fp32, choices in order j = 0..k-1, weights applied at

@@ -1,0 +1,65 @@
+"""The allocation-free expert stage (moe_expert_mlp_noalloc) against the two-call
+stage with a caller buffer for h: bit-identical outputs on two calls in a row,
+and the size limit of its fixed scratch array."""
+from __future__ import annotations
+
+import pytest
+import torch
+
+from combine_moe_layout_gb300 import _binding as B
+from combine_moe_layout_gb300 import pipeline as P
+from combine_moe_layout_gb300 import workloads as wl
+from gpu_common import free_gpu, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "ragged": wl.custom("noalloc_ragged", num_ranks=4, tokens_per_rank=200, hidden=256, num_experts=8, topk=2,
+                        max_m=200, intermediate=384),
+    "tiny": wl.WORKLOADS["tiny"],
+}
+
+
+def _packed(w):
+    step = P.MoeStep(w, "cuda:0")
+    d = P.to_device(wl.make_inputs(w), "cuda:0")
+    step.reset()
+    step.layout(d)
+    step.dispatch(d)
+    packed = B.allocate_packed(step.desc, "cuda:0")
+    step.recv(packed)
+    assert step.error() == B.MOE_OK
+    return step, packed
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_noalloc_matches_the_two_call_stage_twice(name):
+    require_gpu()
+    w = CASES[name]
+    step, packed = _packed(w)
+    rows, H, I = w.num_tokens * w.topk, w.hidden, w.intermediate
+    wts = wl.expert_weights(w, "cuda:0")
+    h = torch.empty((rows, I), dtype=torch.bfloat16, device="cuda:0")
+    y_ref = torch.empty((rows, H), dtype=torch.bfloat16, device="cuda:0")
+    step.expert_mlp(wts, packed, h, y_ref)
+    assert step.error() == B.MOE_OK
+    for _ in range(2):
+        y = torch.full((rows, H), float("nan"), dtype=torch.bfloat16, device="cuda:0")
+        B.moe_expert_mlp_noalloc(step.desc, I, packed.region_offsets, packed.packed_x, wts.w_gate, wts.w_up,
+                                 wts.w_down, y, step.buf.err)
+        assert step.error() == B.MOE_OK
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+    free_gpu()
+
+
+def test_noalloc_rejects_a_stage_above_its_scratch():
+    """The Mixtral shape needs 1.9 GB for h, above the 32 MiB array: MOE_ENOMEM, nothing launched."""
+    require_gpu()
+    w = wl.WORKLOADS["mixtral"]
+    desc = B.MoeDesc.of(w)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    off = torch.zeros(w.num_experts * w.num_ranks + 1, dtype=torch.int32, device="cuda:0")
+    with pytest.raises(B.MoeError) as e:
+        B.moe_expert_mlp_noalloc(desc, w.intermediate, off, None, None, None, None, None, err)
+    assert e.value.status == B.MOE_ENOMEM
+    assert int(err.item()) == 0
