@@ -52,6 +52,34 @@ def test_noalloc_matches_the_two_call_stage_twice(name):
     free_gpu()
 
 
+def test_noalloc_replays_from_a_cuda_graph():
+    """Captured once into a CUDA graph (no allocation happens inside the capture)
+    and replayed twice: bit-identical to the two-call stage each time."""
+    require_gpu()
+    w = CASES["ragged"]
+    step, packed = _packed(w)
+    rows, H, I = w.num_tokens * w.topk, w.hidden, w.intermediate
+    wts = wl.expert_weights(w, "cuda:0")
+    h = torch.empty((rows, I), dtype=torch.bfloat16, device="cuda:0")
+    y_ref = torch.empty((rows, H), dtype=torch.bfloat16, device="cuda:0")
+    step.expert_mlp(wts, packed, h, y_ref)
+    assert step.error() == B.MOE_OK
+    y = torch.empty((rows, H), dtype=torch.bfloat16, device="cuda:0")
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        B.moe_expert_mlp_noalloc(step.desc, I, packed.region_offsets, packed.packed_x, wts.w_gate, wts.w_up,
+                                 wts.w_down, y, step.buf.err)
+    for _ in range(2):
+        y.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert step.error() == B.MOE_OK
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+    free_gpu()
+
+
 def test_noalloc_rejects_a_stage_above_its_scratch():
     """The Mixtral shape needs 1.9 GB for h, above the 32 MiB array: MOE_ENOMEM, nothing launched."""
     require_gpu()
