@@ -94,6 +94,10 @@ def _bind(path: str):
     lib.orc_expert_mlp_row.restype = None
     lib.orc_linear_row.argtypes = [i32, i32, vp, vp, vp]
     lib.orc_linear_row.restype = None
+    lib.orc_linear_row_fp8.argtypes = [i32, i32] + [vp] * 5
+    lib.orc_linear_row_fp8.restype = None
+    lib.orc_gate_up_row_fp8.argtypes = [i32, i32] + [vp] * 9
+    lib.orc_gate_up_row_fp8.restype = None
     lib.orc_validate.argtypes = [i32] * 7
     lib.orc_validate.restype = i32
     lib.orc_buffer_sizes.argtypes = [i32] * 7 + [vp]
@@ -307,6 +311,35 @@ def linear_row(x_bits: np.ndarray, w: np.ndarray) -> np.ndarray:
     y = np.zeros(N, np.uint16)
     _load().orc_linear_row(K, N, _p(x), _p(wm), _p(y))
     return y
+
+
+def linear_row_fp8(xq: np.ndarray, xs: np.ndarray, wq: np.ndarray, ws: np.ndarray) -> np.ndarray:
+    """bf16 bits of y [N] for an fp8 row (codes [K], scales [K/128]) through fp8 weights
+    (codes [N][K], block scales [N/128][K/128])."""
+    x = np.ascontiguousarray(xq, dtype=np.uint8)
+    s = np.ascontiguousarray(xs, dtype=np.float32)
+    w = np.ascontiguousarray(wq, dtype=np.uint8)
+    sw = np.ascontiguousarray(ws, dtype=np.float32)
+    N, K = w.shape
+    y = np.zeros(N, np.uint16)
+    _load().orc_linear_row_fp8(K, N, _p(x), _p(s), _p(w), _p(sw), _p(y))
+    return y
+
+
+def gate_up_row_fp8(xq, xs, wgq, wgs, wuq, wus):
+    """(hv fp64 [I], h codes [I], h scales [I/128]) of linear 1 + SwiGLU for one fp8 row."""
+    x = np.ascontiguousarray(xq, dtype=np.uint8)
+    s = np.ascontiguousarray(xs, dtype=np.float32)
+    wg = np.ascontiguousarray(wgq, dtype=np.uint8)
+    sg = np.ascontiguousarray(wgs, dtype=np.float32)
+    wu = np.ascontiguousarray(wuq, dtype=np.uint8)
+    su = np.ascontiguousarray(wus, dtype=np.float32)
+    I, H = wg.shape
+    hv = np.zeros(I, np.float64)
+    hq = np.zeros(I, np.uint8)
+    hs = np.zeros(I // 128, np.float32)
+    _load().orc_gate_up_row_fp8(H, I, _p(x), _p(s), _p(wg), _p(sg), _p(wu), _p(su), _p(hv), _p(hq), _p(hs))
+    return hv, hq, hs
 
 
 @dataclass

@@ -385,6 +385,57 @@ void orc_expert_mlp_row(int H, int I, const uint16_t *x, const uint16_t *w_gate,
   }
 }
 
+/* The fp8 expert stage. Rows arrive as e4m3 codes with one fp32 scale per 128
+ * contiguous elements (the dispatch format, "NVSHMEM and DeepEP", high-throughput
+ * section). Weights are e4m3 codes with one fp32 scale per 128 x 128 block
+ * (rows n, columns k: scale ws[n / 128][k / 128]). Every value is its code
+ * times its scale, and the products and sums are taken in fp64. */
+
+/* y[n] = bf16( sum_k x[k] w[n][k] ) for one fp8 row x (K codes, K/128 scales)
+ * through an fp8 weight matrix w [N][K] with block scales [N/128][K/128]. */
+void orc_linear_row_fp8(int K, int N, const uint8_t *xq, const float *xs, const uint8_t *wq, const float *ws,
+                        uint16_t *y) {
+  for (int n = 0; n < N; ++n) {
+    double acc = 0.0;
+    for (int k = 0; k < K; ++k) {
+      double xv = orc_e4m3_value(xq[k]) * (double)xs[k / 128];
+      double wv = orc_e4m3_value(wq[(int64_t)n * K + k]) * (double)ws[(int64_t)(n / 128) * (K / 128) + k / 128];
+      acc += xv * wv;
+    }
+    y[n] = orc_bf16_from_double(acc);
+  }
+}
+
+/* Linear 1 with SwiGLU for one fp8 row, h block-quantised for linear 2:
+ *   hv[i] = silu(g) * u (fp64), g and u the fp8 dot products with the gate and
+ *   up rows of the expert; then per 128 contiguous i, with hv rounded to fp32
+ *   (the precision the decision is taken in, as for dispatch): scale =
+ *   amax / 448 (1 for an all-zero block), code = e4m3(hv / scale), fp32 IEEE
+ *   division. hv (fp64) is returned too, for the callers' error bars. */
+void orc_gate_up_row_fp8(int H, int I, const uint8_t *xq, const float *xs, const uint8_t *wgq, const float *wgs,
+                         const uint8_t *wuq, const float *wus, double *hv, uint8_t *hq, float *hs) {
+  for (int i = 0; i < I; ++i) {
+    double g = 0.0, u = 0.0;
+    for (int k = 0; k < H; ++k) {
+      double xv = orc_e4m3_value(xq[k]) * (double)xs[k / 128];
+      int64_t sb = (int64_t)(i / 128) * (H / 128) + k / 128;
+      g += xv * orc_e4m3_value(wgq[(int64_t)i * H + k]) * (double)wgs[sb];
+      u += xv * orc_e4m3_value(wuq[(int64_t)i * H + k]) * (double)wus[sb];
+    }
+    hv[i] = g / (1.0 + exp(-g)) * u;
+  }
+  for (int b = 0; b < I / 128; ++b) {
+    float amax = 0.0f;
+    for (int i = b * 128; i < (b + 1) * 128; ++i) {
+      float v = fabsf((float)hv[i]);
+      if (v > amax) amax = v;
+    }
+    float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+    hs[b] = sc;
+    for (int i = b * 128; i < (b + 1) * 128; ++i) hq[i] = orc_e4m3_from_float((float)hv[i] / sc);
+  }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Cross-node traffic of a routing (per-node deduplication accounting).      */
 /* ------------------------------------------------------------------------ */

@@ -41,13 +41,24 @@ MUTANTS = [
      "int64_t p = (int64_t)region_offsets[region];"),
     ("silu on the up projection", "h[i] = orc_bf16_from_double(g / (1.0 + exp(-g)) * u);",
      "h[i] = orc_bf16_from_double(u / (1.0 + exp(-u)) * g);"),
-    ("silu sign", "g / (1.0 + exp(-g))", "g / (1.0 + exp(g))"),
+    ("silu sign", "h[i] = orc_bf16_from_double(g / (1.0 + exp(-g)) * u);",
+     "h[i] = orc_bf16_from_double(g / (1.0 + exp(g)) * u);"),
+    ("fp8 silu sign", "hv[i] = g / (1.0 + exp(-g)) * u;", "hv[i] = g / (1.0 + exp(g)) * u;"),
     ("gate weight transposed", "g += xv * orc_bf16_value(w_gate[(int64_t)i * H + k]);",
      "g += xv * orc_bf16_value(w_gate[(int64_t)k * I + i]);"),
     ("down weight transposed", "acc += orc_bf16_value(h[i]) * orc_bf16_value(w_down[(int64_t)j * I + i]);",
      "acc += orc_bf16_value(h[i]) * orc_bf16_value(w_down[(int64_t)i * H + j]);"),
     ("linear weight transposed", "acc += orc_bf16_value(x[k]) * orc_bf16_value(w[(int64_t)n * K + k]);",
      "acc += orc_bf16_value(x[k]) * orc_bf16_value(w[(int64_t)k * N + n]);"),
+    ("fp8 weight block scale transposed",
+     "double wv = orc_e4m3_value(wq[(int64_t)n * K + k]) * (double)ws[(int64_t)(n / 128) * (K / 128) + k / 128];",
+     "double wv = orc_e4m3_value(wq[(int64_t)n * K + k]) * (double)ws[(int64_t)(k / 128) * (K / 128) + n / 128];"),
+    ("fp8 row scale dropped", "double xv = orc_e4m3_value(xq[k]) * (double)xs[k / 128];\n      double wv",
+     "double xv = orc_e4m3_value(xq[k]);\n      double wv"),
+    ("fp8 gate block scale index", "int64_t sb = (int64_t)(i / 128) * (H / 128) + k / 128;",
+     "int64_t sb = (int64_t)(i % 128) % (H / 128) + k / 128;"),
+    ("fp8 h scale off", "float sc = amax > 0.0f ? amax / 448.0f : 1.0f;\n    hs[b] = sc;",
+     "float sc = amax > 0.0f ? amax / 440.0f : 1.0f;\n    hs[b] = sc;"),
     ("quantiser scale off", "float s = amax > 0.0f ? amax / 448.0f : 1.0f;", "float s = amax > 0.0f ? amax / 447.0f : 1.0f;"),
 ]
 
@@ -74,6 +85,9 @@ PINS = [
     lambda: pins.test_expert_mlp_row_is_zero_for_zero_gate(None),
     lambda: pins.test_expert_mlp_row_matches_a_library_matmul(None),
     lambda: pins.test_linear_row_matches_a_library_matmul_and_an_identity(None),
+    lambda: pins.test_linear_row_fp8_unit_scales_identity(None),
+    lambda: pins.test_linear_row_fp8_matches_a_library_matmul(None),
+    lambda: pins.test_gate_up_row_fp8_matches_library_ops(None),
 ]
 
 

@@ -482,3 +482,68 @@ def test_linear_row_matches_a_library_matmul_and_an_identity(oracle_lib):
     # a permutation matrix permutes
     perm = rng.permutation(K)
     assert (oracle.linear_row(x, _bf16(np.eye(K)[perm])) == x[perm]).all()
+
+
+# --- the fp8 expert stage ------------------------------------------------------
+
+def _e4m3(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+
+
+def _fp8_case(rng, K, N):
+    xq = rng.integers(0, 256, K, dtype=np.uint8)
+    xq[(xq & 0x7F) == 0x7F] = 0x38                           # no NaN codes
+    wq = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    wq[(wq & 0x7F) == 0x7F] = 0x30
+    xs = rng.uniform(0.5, 2.0, K // 128).astype(np.float32) * 2.0 ** -6
+    ws = rng.uniform(0.5, 2.0, (N // 128, K // 128)).astype(np.float32) * 2.0 ** -7
+    return xq, xs, wq, ws
+
+
+def _dequant_rows(wq, ws):
+    N, K = wq.shape
+    return _e4m3(wq) * np.repeat(np.repeat(ws.astype(np.float64), 128, 0), 128, 1)[:N, :K]
+
+
+def test_linear_row_fp8_matches_a_library_matmul(oracle_lib):
+    """y = bf16((x * xs) . (w * ws)) within one bf16 rounding of numpy's fp64 product over
+    torch's e4m3 decode; block scales indexed [n / 128][k / 128]."""
+    rng = np.random.default_rng(40)
+    K, N = 256, 384
+    xq, xs, wq, ws = _fp8_case(rng, K, N)
+    y = oracle.linear_row_fp8(xq, xs, wq, ws)
+    x = _e4m3(xq) * np.repeat(xs.astype(np.float64), 128)
+    yf = _dequant_rows(wq, ws) @ x
+    assert (np.abs(_val(y) - yf) <= np.abs(yf) * 2.0 ** -8 * 1.0001).all()
+
+
+def test_linear_row_fp8_unit_scales_identity(oracle_lib):
+    """Identity codes (1.0 = 0x38) with unit scales return the row's values, rounded to bf16 (exact for e4m3)."""
+    rng = np.random.default_rng(41)
+    K = 256
+    xq = rng.integers(0, 256, K, dtype=np.uint8)
+    xq[(xq & 0x7F) == 0x7F] = 0
+    wq = np.where(np.eye(K, dtype=bool), np.uint8(0x38), np.uint8(0)).astype(np.uint8)
+    y = oracle.linear_row_fp8(xq, np.ones(K // 128, np.float32), wq, np.ones((K // 128, K // 128), np.float32))
+    x = _e4m3(xq)
+    assert np.array_equal(_val(y), x)      # every e4m3 value is a bf16 value (signed zeros compare equal)
+
+
+def test_gate_up_row_fp8_matches_library_ops(oracle_lib):
+    """hv = silu(g) u from numpy fp64 products and torch's silu; the h codes equal torch's
+    float8_e4m3fn cast of fp32(hv) / (amax / 448) in fp32, per 128-block."""
+    rng = np.random.default_rng(42)
+    H, I = 256, 384
+    xq, xs, wgq, wgs = _fp8_case(rng, H, I)
+    _, _, wuq, wus = _fp8_case(rng, H, I)
+    hv, hq, hs = oracle.gate_up_row_fp8(xq, xs, wgq, wgs, wuq, wus)
+    x = _e4m3(xq) * np.repeat(xs.astype(np.float64), 128)
+    g, u = _dequant_rows(wgq, wgs) @ x, _dequant_rows(wuq, wus) @ x
+    want = torch.nn.functional.silu(torch.from_numpy(g)).numpy() * u
+    assert np.allclose(hv, want, rtol=1e-12, atol=1e-300)
+    hf = torch.from_numpy(hv.astype(np.float32)).view(I // 128, 128)
+    amax = hf.abs().amax(dim=1)
+    sc = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    assert np.array_equal(hs, sc.numpy())
+    codes = (hf / sc[:, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy().ravel()
+    assert np.array_equal(hq, codes)
