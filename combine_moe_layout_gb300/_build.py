@@ -22,7 +22,7 @@ STAMP = os.path.join(LIBDIR, "libmoe_layout.stamp")
 
 SOURCES = ["moe_layout.cu", "moe_dispatch.cu", "moe_layout_dispatch.cu", "moe_recv.cu", "moe_combine.cu",
            "moe_expert_stub.cu", "moe_route_stats.cu", "moe_expert.cu",
-           "moe_expert_noalloc.cu"]
+           "moe_expert_noalloc.cu", "moe_expert_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

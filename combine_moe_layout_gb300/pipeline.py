@@ -124,5 +124,17 @@ class MoeStep:
                              weights.w_up, h, b.err, stream)
         B.moe_expert_down(self.desc, weights.inter, packed.region_offsets, h, weights.w_down, packed_y, b.err, stream)
 
+    def expert_mlp_fp8(self, weights, packed: B.PackedBuffers, h: torch.Tensor, h_scales: torch.Tensor,
+                       packed_y: torch.Tensor, stream=None):
+        """The fp8 expert stage on e4m3 packed rows: linear 1 with SwiGLU into h
+        (e4m3 [R*T*k][I]) and h_scales ([R*T*k][I/128]), then linear 2 into
+        packed_y [R*T*k][H] bf16."""
+        b = self.buf
+        B.moe_expert_gate_up_fp8(self.desc, weights.inter, packed.region_offsets, packed.packed_x,
+                                 packed.packed_scales, weights.w_gate, weights.w_gate_scales, weights.w_up,
+                                 weights.w_up_scales, h, h_scales, b.err, stream)
+        B.moe_expert_down_fp8(self.desc, weights.inter, packed.region_offsets, h, h_scales, weights.w_down,
+                              weights.w_down_scales, packed_y, b.err, stream)
+
     def error(self, stream=None) -> int:
         return B.moe_get_error(self.buf.err, stream)

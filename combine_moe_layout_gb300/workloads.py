@@ -278,3 +278,51 @@ def expert_weights(w: Workload, device="cpu", seed: int | None = None, inter: in
         return t.mul_(fan_in ** -0.5).to(torch.bfloat16)
 
     return ExpertWeights(I, draw((E, I, H), H), draw((E, I, H), H), draw((E, H, I), I))
+
+
+@dataclass
+class ExpertWeightsFp8:
+    inter: int
+    w_gate: torch.Tensor         # [E][I][H] uint8 e4m3 codes
+    w_gate_scales: torch.Tensor  # [E][I/128][H/128] float32
+    w_up: torch.Tensor
+    w_up_scales: torch.Tensor
+    w_down: torch.Tensor         # [E][H][I] uint8
+    w_down_scales: torch.Tensor  # [E][H/128][I/128] float32
+
+
+def _block_quantize_e4m3(v: torch.Tensor):
+    """e4m3 codes and one fp32 scale per 128 x 128 block of [n][N][K] values
+    (scale = block amax / 448, 1 for an all-zero block; torch's nearest-even cast)."""
+    n, N, K = v.shape
+    b = v.view(n, N // 128, 128, K // 128, 128)
+    amax = b.abs().amax(dim=(2, 4))
+    sc = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    q = (b / sc[:, :, None, :, None]).clamp_(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).view(n, N, K), sc.float()
+
+
+def expert_weights_fp8(w: Workload, device="cpu", seed: int | None = None, inter: int | None = None,
+                       chunk: int = 16) -> ExpertWeightsFp8:
+    """Synthetic fp8 expert weights: N(0, 1/K) draws (torch's generator on
+    `device`, gate then up then down, `chunk` experts at a time) block-quantised
+    to e4m3 with one fp32 scale per 128 x 128 block."""
+    I = w.intermediate if inter is None else inter
+    E, H = w.num_experts, w.hidden
+    g = torch.Generator(device=device)
+    g.manual_seed((w.seed if seed is None else seed) + 104729)
+
+    def draw(N, K):
+        q = torch.empty((E, N, K), dtype=torch.uint8, device=device)
+        s = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device=device)
+        for e0 in range(0, E, chunk):
+            e1 = min(E, e0 + chunk)
+            v = torch.randn((e1 - e0, N, K), generator=g, device=device, dtype=torch.float32).mul_(K ** -0.5)
+            q[e0:e1], s[e0:e1] = _block_quantize_e4m3(v)
+            del v
+        return q, s
+
+    wg, sg = draw(I, H)
+    wu, su = draw(I, H)
+    wd, sd = draw(H, I)
+    return ExpertWeightsFp8(I, wg, sg, wu, su, wd, sd)

@@ -244,6 +244,39 @@ moe_status moe_expert_gate_up(const moe_desc *desc, int32_t inter, const int32_t
 moe_status moe_expert_down(const moe_desc *desc, int32_t inter, const int32_t *region_offsets, const void *h,
                            const void *w_down, void *packed_y, int32_t *err, void *stream);
 
+/* Expert stage on fp8 rows, linear 1 with SwiGLU (the passages of
+ * moe_expert_gate_up; "NVSHMEM and DeepEP", high-throughput section, for rows
+ * sent as FP8 with one fp32 scale per 128 elements). A row's value is its e4m3
+ * code times its block scale; weights are e4m3 codes with one fp32 scale per
+ * 128 x 128 block. For every packed row p of expert e:
+ *   hv[p][i] = silu(g) * u,  g = sum_c x[p][c] w_gate[e][i][c],  u alike,
+ * fp32 accumulation on the tensor cores (code products per 128-wide K block,
+ * then times the two scales); then per 128 contiguous i, in fp32:
+ *   h_scales[p][i/128] = amax / 448 (1 for an all-zero block),
+ *   h[p][i] = e4m3(hv / scale), round to nearest even, saturating at 448.
+ *   desc: dtype MOE_FP8_E4M3 or MOE_BF16_TO_FP8 (the packed rows are e4m3),
+ *   H a multiple of 128; inter I a multiple of 128.
+ *   packed_x [R*T*k][H] e4m3 and packed_scales [R*T*k][H/128] f32 (as
+ *   moe_dispatch_recv writes them); w_gate, w_up [E][I][H] e4m3 with
+ *   w_gate_scales, w_up_scales [E][I/128][H/128] f32; h [R*T*k][I] e4m3 and
+ *   h_scales [R*T*k][I/128] f32 (written for packed rows only). Row and weight
+ *   pointers 16-byte aligned, scale pointers 4-byte aligned.
+ * Errors as moe_expert_gate_up (MOE_EINVAL for bf16 rows). */
+moe_status moe_expert_gate_up_fp8(const moe_desc *desc, int32_t inter, const int32_t *region_offsets,
+                                  const void *packed_x, const float *packed_scales, const void *w_gate,
+                                  const float *w_gate_scales, const void *w_up, const float *w_up_scales, void *h,
+                                  float *h_scales, int32_t *err, void *stream);
+
+/* Expert stage on fp8 rows, linear 2: for every packed row p of expert e,
+ *   packed_y[p][j] = bf16_rne( sum_i h[p][i] w_down[e][j][i] ),
+ * with h as moe_expert_gate_up_fp8 writes it and w_down [E][H][I] e4m3 with
+ * w_down_scales [E][H/128][I/128] f32; fp32 accumulation on the tensor cores.
+ * packed_y [R*T*k][H] bf16 is what moe_combine_packed reads. Sizes, alignment
+ * and errors as moe_expert_gate_up_fp8. */
+moe_status moe_expert_down_fp8(const moe_desc *desc, int32_t inter, const int32_t *region_offsets, const void *h,
+                               const float *h_scales, const void *w_down, const float *w_down_scales,
+                               void *packed_y, int32_t *err, void *stream);
+
 /* The expert stage (moe_expert_gate_up then moe_expert_down) in one call that
  * allocates nothing. The pages have no counterpart of this call: it exists for
  * callers that may not allocate device memory. h is kept in a fixed device array
