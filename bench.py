@@ -464,25 +464,34 @@ def run_expert(args, rank, local_rank, world):
         I_ = args.intermediate or w.intermediate
         w = replace(w, name=f"{w.name}_T{T_}_I{I_}", tokens_per_rank=T_, max_m=T_, intermediate=I_)
         wl.DESCRIPTIONS.setdefault(w.name, f"{wl.DESCRIPTIONS[args.workload]}; {T_} tokens per rank, I {I_}")
-    if w.dtype != "bf16":
-        raise SystemExit(f"--expert needs a bf16 workload, {w.name} is {w.dtype}")
+    fp8 = w.dtype != "bf16"   # e4m3 rows: the fp8 expert stage with fp8 weights
     inp = wl.make_inputs(w)
     step = P.MoeStep(w, dev, args.num_sms)
     d = P.to_device(inp, dev)
-    wts = wl.expert_weights(w, dev)
+    wts = wl.expert_weights_fp8(w, dev) if fp8 else wl.expert_weights(w, dev)
     packed = B.allocate_packed(step.desc, dev)
     rows, H, I = w.num_tokens * w.topk, w.hidden, w.intermediate
-    h = torch.empty((rows, I), dtype=torch.bfloat16, device=dev)
+    h = torch.empty((rows, I), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+    hs = torch.empty((rows, I // 128), dtype=torch.float32, device=dev) if fp8 else None
     y = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
     step.reset()
 
+    if fp8:
+        gate_up = lambda dd, out=None: B.moe_expert_gate_up_fp8(  # noqa: E731
+            step.desc, I, packed.region_offsets, packed.packed_x, packed.packed_scales, wts.w_gate,
+            wts.w_gate_scales, wts.w_up, wts.w_up_scales, h, hs, step.buf.err)
+        down = lambda dd, out=None: B.moe_expert_down_fp8(  # noqa: E731
+            step.desc, I, packed.region_offsets, h, hs, wts.w_down, wts.w_down_scales, y, step.buf.err)
+    else:
+        gate_up = lambda dd, out=None: B.moe_expert_gate_up(  # noqa: E731
+            step.desc, I, packed.region_offsets, packed.packed_x, wts.w_gate, wts.w_up, h, step.buf.err)
+        down = lambda dd, out=None: B.moe_expert_down(  # noqa: E731
+            step.desc, I, packed.region_offsets, h, wts.w_down, y, step.buf.err)
     stages = [("layout_dispatch", lambda dd, out=None: step.layout_dispatch(dd)),
               ("recv", lambda dd, out=None: step.recv(packed)),
-              ("expert_gate_up", lambda dd, out=None: B.moe_expert_gate_up(
-                  step.desc, I, packed.region_offsets, packed.packed_x, wts.w_gate, wts.w_up, h, step.buf.err)),
-              ("expert_down", lambda dd, out=None: B.moe_expert_down(
-                  step.desc, I, packed.region_offsets, h, wts.w_down, y, step.buf.err)),
+              ("expert_gate_up", gate_up),
+              ("expert_down", down),
               ("combine_packed", lambda dd, out=None: step.combine_packed(dd, y, packed, out=out))]
 
     def path(dd, out=None):
@@ -540,7 +549,8 @@ def run_expert(args, rank, local_rank, world):
             path(hd, out=hout)
             eev[i][1].record(stream)
         torch.cuda.synchronize()
-        nbytes = inp.x.nbytes + inp.topk_idx.nbytes + inp.topk_weights.nbytes
+        nbytes = inp.x.nbytes + inp.topk_idx.nbytes + inp.topk_weights.nbytes + \
+            (inp.x_scales.nbytes if inp.x_scales is not None else 0)
         e2e = {"value": None, "unit": "tokens/s", "h2d_bytes_per_step": int(nbytes),
                "d2h_bytes_per_step": hout.numel() * 2,
                "local_ms_total": sum(a.elapsed_time(b) for a, b in eev),
@@ -565,14 +575,23 @@ def run_expert(args, rank, local_rank, world):
     # that received rows, the packed input rows, the output rows
     used = int((packed.region_offsets[w.num_ranks::w.num_ranks].cpu() -
                 packed.region_offsets[:-1:w.num_ranks].cpu() > 0).sum())
-    gbytes = {"expert_gate_up": used * 2 * I * H * 2 + rows * H * 2 + rows * I * 2,
-              "expert_down": used * H * I * 2 + rows * I * 2 + rows * H * 2}
-    weight_bytes = 3 * w.num_experts * I * H * 2
+    if fp8:   # e4m3 weights, rows and h, with their fp32 block scales; bf16 y
+        gbytes = {"expert_gate_up": used * 2 * (I * H + I * H // 128 // 128 * 4) + rows * (H + H // 128 * 4) +
+                  rows * (I + I // 128 * 4),
+                  "expert_down": used * (H * I + H * I // 128 // 128 * 4) + rows * (I + I // 128 * 4) + rows * H * 2}
+        weight_bytes = 3 * w.num_experts * I * H
+    else:
+        gbytes = {"expert_gate_up": used * 2 * I * H * 2 + rows * H * 2 + rows * I * 2,
+                  "expert_down": used * H * I * 2 + rows * I * 2 + rows * H * 2}
+        weight_bytes = 3 * w.num_experts * I * H * 2
     burst, sustained, kind = measured_tensor_peak()
+    if fp8:   # the fp8 tensor rate: the measured bf16 rate times the nominal fp8 / bf16 ratio (4.5 / 2.25)
+        burst, sustained, kind = 2 * burst, 2 * sustained, kind + " bf16 x 2 (nominal fp8/bf16 ratio)"
     hbm, hbm_kind = measured_hbm_peak()
     top = max(flops, key=lambda n: kern_ms[n])
     # the kernel's bound: whichever of its flops and its bytes takes longer at the measured peaks
     tensor_bound = flops[top] / (sustained * 1e12) >= gbytes[top] / (hbm * 1e9)
+    kname = "grouped_gemm_fp8_kernel" if fp8 else "grouped_gemm_kernel"
     ab = dict(w.algorithmic_bytes())
     kernel_stats = {}
     for name, ms in kern_ms.items():
@@ -580,8 +599,8 @@ def run_expert(args, rank, local_rank, world):
         if name in flops:
             tf = flops[name] / (ms / 1e3) / 1e12
             gbs = gbytes[name] / (ms / 1e3) / 1e9
-            st.update({"flops": flops[name], "TFLOPs": round(tf, 1), "frac_of_sustained_bf16": round(tf / sustained, 4),
-                       "frac_of_burst_bf16": round(tf / burst, 4), "algorithmic_bytes": gbytes[name],
+            st.update({"flops": flops[name], "TFLOPs": round(tf, 1), "frac_of_sustained_tensor": round(tf / sustained, 4),
+                       "frac_of_burst_tensor": round(tf / burst, 4), "algorithmic_bytes": gbytes[name],
                        "GBps": round(gbs, 1), "frac_of_measured_hbm": round(gbs / hbm, 4)})
         else:
             key = {"layout_dispatch": None, "recv": "recv", "combine_packed": "combine_packed"}[name]
@@ -591,29 +610,33 @@ def run_expert(args, rank, local_rank, world):
     line = {
         "metric": METRIC, "value": round(job["value"], 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": round(job["ms_per_step"], 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "impl": "native",
+        "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16", "data": "synthetic", "impl": "native",
         "config": {
             "workload": w.name + "+experts", "description": wl.DESCRIPTIONS[w.name],
-            "expert_mlp": f"{w.num_experts} experts, linear 1 {H}->2x{I} with SwiGLU, linear 2 {I}->{H}, bf16 "
+            "expert_mlp": f"{w.num_experts} experts, linear 1 {H}->2x{I} with SwiGLU, linear 2 {I}->{H}, "
+                          + ("e4m3 weights with 128x128 fp32 block scales, h e4m3 with 128-element scales, "
+                             if fp8 else "bf16 ") +
                           f"weights N(0,1/K) ({weight_bytes / 1e9:.2f} GB resident)",
             "tokens_per_step_per_gpu": w.num_tokens, "flops_per_step": sum(flops.values()),
             "path": "fused layout+dispatch -> receive hook (expert-major packing) -> linear 1 + SwiGLU -> linear 2 "
-                    "(tcgen05 grouped GEMMs, fp32 accumulate) -> packed combine",
+                    + ("(tcgen05 kind::f8f6f4 grouped GEMMs, fp32 block-scale promotion) " if fp8 else
+                       "(tcgen05 grouped GEMMs, fp32 accumulate) ") + "-> packed combine",
             "l2": "flushed before every timed step, outside the timed events",
             "launch": "direct launches through the C ABI",
             "parallelism": "replicas only: one independent EP group per GPU",
         },
-        "roofline": ({"kernel": "grouped_gemm_kernel (" + top + ")", "bound": "tensor",
+        "roofline": ({"kernel": kname + " (" + top + ")", "bound": "tensor",
                       "achieved": kernel_stats[top]["TFLOPs"], "peak": sustained,
-                      "peak_kind": f"{kind} bf16 dense, sustained (the kernel runs inside a multi-ms step)",
-                      "unit": "TFLOP/s", "frac": kernel_stats[top]["frac_of_sustained_bf16"],
-                      "frac_of_burst": kernel_stats[top]["frac_of_burst_bf16"],
-                      "traffic": profiled_traffic("moe_expert.cu", w.name),
+                      "peak_kind": f"{kind} {'fp8' if fp8 else 'bf16'} dense, sustained (the kernel runs inside a "
+                                   "multi-ms step)",
+                      "unit": "TFLOP/s", "frac": kernel_stats[top]["frac_of_sustained_tensor"],
+                      "frac_of_burst": kernel_stats[top]["frac_of_burst_tensor"],
+                      "traffic": profiled_traffic("moe_expert_fp8.cu" if fp8 else "moe_expert.cu", w.name),
                       "algorithmic_flops_per_launch": flops[top]} if tensor_bound else
-                     {"kernel": "grouped_gemm_kernel (" + top + ")", "bound": "hbm",
+                     {"kernel": kname + " (" + top + ")", "bound": "hbm",
                       "achieved": kernel_stats[top]["GBps"], "peak": hbm, "peak_kind": f"{hbm_kind} (copy bandwidth)",
                       "unit": "GB/s", "frac": kernel_stats[top]["frac_of_measured_hbm"],
-                      "traffic": profiled_traffic("moe_expert.cu", w.name),
+                      "traffic": profiled_traffic("moe_expert_fp8.cu" if fp8 else "moe_expert.cu", w.name),
                       "algorithmic_bytes_per_launch": gbytes[top]}),
         "kernels": kernel_stats,
         "kernel_timing": "CUDA events between the launches, a second pass of the same K steps",
@@ -636,22 +659,48 @@ def cpu_baseline_expert(w, inp, seconds: float) -> dict:
     t0 = time.perf_counter()
     oracle.layout(inp.topk_idx, w.num_experts, w.max_m)
     t_layout = time.perf_counter() - t0
-    wts = wl.expert_weights(w, "cpu")
-    bits = [t.view(torch.int16).numpy().view(np.uint16) for t in (wts.w_gate, wts.w_up, wts.w_down)]
     x = inp.x.reshape(w.num_tokens, w.hidden)
     idx = inp.topk_idx.reshape(w.num_tokens, w.topk)
+    H, I = w.hidden, w.intermediate
+    if w.dtype == "bf16":
+        wts = wl.expert_weights(w, "cpu")
+        bits = [t.view(torch.int16).numpy().view(np.uint16) for t in (wts.w_gate, wts.w_up, wts.w_down)]
+
+        def row(tok, e):
+            oracle.expert_mlp_row(x[tok], bits[0][e], bits[1][e], bits[2][e])
+        weights = "the workload's synthetic bf16 weights"
+    else:
+        # the oracle's cost does not depend on the weight values: random e4m3 codes and unit block scales
+        # for the experts the sampled tokens reach (generating all of the fp8 weights on the host would
+        # take longer than the sample)
+        xs = inp.x_scales.reshape(w.num_tokens, H // 128)
+        rng = np.random.default_rng(0)
+        cache = {}
+
+        def weights_of(e):
+            if e not in cache:
+                q = [rng.integers(0, 0x7E, shape, dtype=np.uint8) for shape in ((I, H), (I, H), (H, I))]
+                sc = [np.ones((a.shape[0] // 128, a.shape[1] // 128), np.float32) for a in q]
+                cache[e] = (q, sc)
+            return cache[e]
+
+        def row(tok, e):
+            (wg, wu, wd), (sg, su, sd) = weights_of(int(e))
+            hv, hq, hs = oracle.gate_up_row_fp8(x[tok], xs[tok], wg, sg, wu, su)
+            oracle.linear_row_fp8(hq, hs, wd, sd)
+        weights = "random e4m3 weight codes (the oracle's cost does not depend on them)"
     spent, n = 0.0, 0
     while n < 1 or spent < seconds:
         tok = (n * 7919) % w.num_tokens
         t0 = time.perf_counter()
         for e in idx[tok]:
-            oracle.expert_mlp_row(x[tok], bits[0][e], bits[1][e], bits[2][e])
+            row(tok, e)
         spent += time.perf_counter() - t0
         n += 1
     per_tok = spent / n + t_layout / w.num_tokens
     return {"value": round(1.0 / per_tok, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"layout of all {w.num_tokens} tokens + the {w.topk} expert MLP rows of {n} tokens, "
-                      f"single-threaded C oracle (fp64)", "seconds": round(spent + t_layout, 2),
+                      f"single-threaded C oracle (fp64), {weights}", "seconds": round(spent + t_layout, 2),
             "cpu": _cpu_model()}
 
 
@@ -793,7 +842,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=("native", "reference"), default="native")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", default=None, help=f"default {DEFAULT_WORKLOAD} (mixtral with --expert)")
     ap.add_argument("--num-sms", type=int, default=0)
     ap.add_argument("--unfused", action="store_true", help="time layout and dispatch as two calls")
     ap.add_argument("--graph", action="store_true", help="replay the step's launches from a CUDA graph")
@@ -812,8 +861,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)
-    if args.expert and args.workload == DEFAULT_WORKLOAD:
-        args.workload = "mixtral"
+    if args.workload is None:
+        args.workload = "mixtral" if args.expert else DEFAULT_WORKLOAD
     if args.steps is None:
         args.steps = (50 if args.expert else 2000) if args.impl == "native" else 20
     if args.warmup is None:

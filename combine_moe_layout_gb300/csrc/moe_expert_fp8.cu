@@ -19,14 +19,16 @@
 //             so linear 2 reads e4m3 rows with 128-element scales.
 //   down:     y = bf16(sum), round to nearest even.
 //
-// Kernel shape: one persistent CTA per SM, 320 threads.
+// Kernel shape: one persistent CTA per SM, 384 threads in three warpgroups;
+// warpgroup 0 runs with 56 registers a thread and the others with 224
+// (setmaxnreg), so the promotion warps keep 128 fp32 sums in registers.
 //   warp 0      TMA producer: a 128-row x 128-byte A tile and a 256-row B tile
 //               per K block (one scale block), 128-byte swizzle, 4 stages.
 //   warp 1      owns 512 TMEM columns (two 128 x 256 fp32 partials) and issues
 //               4 MMAs (M 128, N 256 or 128, K 32) per K block into one
 //               partial, alternating partials so the next K block's MMAs run
-//               while the previous partial is promoted.
-//   warps 2-9   promotion and epilogue: warp w reads TMEM lanes 32 (w % 4) ..
+//               while the previous partial is promoted. Warps 2-3 idle.
+//   warps 4-11  promotion and epilogue: warp w reads TMEM lanes 32 (w % 4) ..
 //               +31 (the tile's rows) and one half of the columns; it adds the
 //               scaled partial into 128 fp32 registers and, after the last K
 //               block, stores the row's part of the tile. For gate/up a warp
@@ -54,7 +56,14 @@ constexpr int kF8TileB = kF8BN * kF8BK;         // 32 KB
 constexpr int kF8Stage = kF8TileA + kF8TileB;
 constexpr int kF8BoxBytes = kBoxRows * kF8BK;   // one 128 x 128-byte box
 constexpr int kF8PromoWarps = 8;
-constexpr int kF8Threads = 64 + 32 * kF8PromoWarps;
+constexpr int kF8Threads = 128 + 32 * kF8PromoWarps;  // warpgroup 0: TMA, MMA (+2 idle); warpgroups 1-2: promotion
+// Register split by warpgroup (setmaxnreg): the block is launched with 168
+// registers a thread (384 threads x 168 = 64512); warpgroup 0 gives back to 56
+// and the two promotion warpgroups take 224: 128 x 56 + 256 x 224 = 64512.
+constexpr int kF8LaunchRegs = 168;
+constexpr int kF8CtrlRegs = 56;
+constexpr int kF8PromoRegs = 224;
+static_assert(128 * kF8CtrlRegs + 256 * kF8PromoRegs <= kF8Threads * kF8LaunchRegs, "register split over budget");
 constexpr uint32_t kF8TmemCols = 2 * kF8BN;     // two partials
 // stages | full, empty (S each), pfull, pempty (2 each), xbar (4), done | slot, abort | amax exchange
 constexpr int kF8Bars = 2 * kF8Stages + 2 + 2 + 4 + 1;
@@ -104,6 +113,28 @@ struct F8Args {
 // cbase: gate/up puts chunks 2 and 3 on the up columns, 128 further on.
 __device__ __forceinline__ int chunk_col(bool swiglu, int cbase, int c) {
   return swiglu ? (c < 2 ? cbase + 32 * c : 128 + cbase + 32 * (c - 2)) : cbase + 32 * c;
+}
+
+template <int N>
+__device__ __forceinline__ void regs_release() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void regs_claim() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// acc[0..1] = f * p[0..1] + acc[0..1], one packed fp32 FMA (each lane rounded as fmaf).
+__device__ __forceinline__ void fma2(float f, uint32_t p0, uint32_t p1, float &a0, float &a1) {
+  asm("{\n\t.reg .b64 s, x, c, d;\n\t"
+      "mov.b64 s, {%2, %2};\n\t"
+      "mov.b64 x, {%3, %4};\n\t"
+      "mov.b64 c, {%0, %1};\n\t"
+      "fma.rn.f32x2 d, s, x, c;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(f), "r"(p0), "r"(p1));
 }
 
 __device__ __forceinline__ void mbar_arrive_local(uint64_t *bar) {
@@ -163,6 +194,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   const int kblocks = a.K / kF8BK;
 
   if (warp == 0) {
+    regs_release<kF8CtrlRegs>();
     if (lane == 0) {
       // ---- TMA producer ----
       uint32_t it = 0;
@@ -197,6 +229,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
+    regs_release<kF8CtrlRegs>();
     if (lane == 0) {
       // ---- MMA issuer: one partial per K block, two partials alternating ----
       uint32_t it = 0, pk = 0;
@@ -226,10 +259,13 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       mbar_wait_bounded(done, 0);
     }
     __syncwarp();
+  } else if (warp < 4) {
+    regs_release<kF8CtrlRegs>();  // warps 2-3: idle
   } else {
-    // ---- promotion and epilogue: warps 2..9 ----
+    regs_claim<kF8PromoRegs>();
+    // ---- promotion and epilogue: warps 4..11 ----
     const int q = warp & 3;              // TMEM lane quarter this warp may access
-    const int j = (warp - 2) >> 2;       // column half
+    const int j = (warp - 4) >> 2;       // column half
     const int m = q * 32 + lane;         // row within the tile
     const int k128 = a.K / kF8BK;
     // the 32-column chunks this warp promotes: gate/up takes gate columns
@@ -251,10 +287,19 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 #pragma unroll
       for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
       bool ok = true;
+      // the K block's scales, loaded one K block ahead
+      const float *sa_p = a.a_scales + arow * k128, *sb_p = a.b_scales + blk * k128;
+      const float *sb2_p = a.b2_scales + blk * k128;
+      float sa_n = __ldg(sa_p), sb_n = __ldg(sb_p), sb2_n = sw ? __ldg(sb2_p) : 0.0f;
       for (int kb = 0; kb < kblocks; ++kb, ++pk) {
-        const float sa = __ldg(a.a_scales + arow * k128 + kb);
-        const float f0 = sa * __ldg(a.b_scales + blk * k128 + kb);
-        const float f1 = a.swiglu ? sa * __ldg(a.b2_scales + blk * k128 + kb) : f0;
+        const float sa = sa_n, sb = sb_n, sb2 = sb2_n;
+        if (kb + 1 < kblocks) {
+          sa_n = __ldg(sa_p + kb + 1);
+          sb_n = __ldg(sb_p + kb + 1);
+          if (sw) sb2_n = __ldg(sb2_p + kb + 1);
+        }
+        const float f0 = sa * sb;
+        const float f1 = sw ? sa * sb2 : f0;
         const uint32_t pb = pk & 1u, pph = (pk >> 1) & 1u;
         int got = 0;
         if (lane == 0) got = role_wait(pfull + pb, pph, abort, a.err) ? 1 : 0;
@@ -266,11 +311,11 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         tc_fence_after();
         const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * kF8BN;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 4; c += 2) {
           if (c < ncol) {
-            uint32_t r[32];
-            tmem_load32_wait(tb + chunk_col(sw, cbase, c), r);
-            if (c == ncol - 1) {
+            uint32_t r[64];
+            tmem_load32x2_wait(tb + chunk_col(sw, cbase, c), tb + chunk_col(sw, cbase, c + 1), r);
+            if (c + 2 >= ncol) {
               // the partial has been read: the MMA warp may refill it
               tc_fence_before();
               __syncwarp();
@@ -278,7 +323,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             }
             const float f = (sw && c >= 2) ? f1 : f0;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[32 * c + i] = fmaf(f, __uint_as_float(r[i]), acc[32 * c + i]);
+            for (int i = 0; i < 64; i += 2) fma2(f, r[i], r[i + 1], acc[32 * c + i], acc[32 * c + i + 1]);
           }
         }
       }
@@ -362,6 +407,10 @@ moe_status launch_fp8(F8Args a, const void *A, const void *B0, const void *B1, i
     return MOE_ECUDA;
   if (cudaFuncSetAttribute(grouped_gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
+    return MOE_ECUDA;
+  // the register split needs the launch allocation it was sized for
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, grouped_gemm_fp8_kernel) != cudaSuccess || fa.numRegs < kF8LaunchRegs)
     return MOE_ECUDA;
   const int64_t grid = max_tiles < sms ? max_tiles : sms;
   if (grid <= 0) return MOE_OK;

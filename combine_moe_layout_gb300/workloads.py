@@ -104,6 +104,9 @@ WORKLOADS = {
                        intermediate=2048),
     "ds_prefill": Workload("ds_prefill", 8, 4096, 7168, 256, 8, 4096, "fp8", "group", True, "scale", "normal",
                            intermediate=2048),
+    # the Mixtral shape with fp8 rows (the fp8 expert stage at 8192 rows per expert)
+    "mixtral_fp8": Workload("mixtral_fp8", 8, 4096, 4096, 8, 2, 4096, "fp8", "softmax", True, "scale", "normal",
+                            intermediate=14336),
     # the decode shape with bf16 rows quantised to fp8 + scales on dispatch
     "ds_decode_bf16in": Workload("ds_decode_bf16in", 8, 128, 7168, 256, 8, 128, "bf16q", "softmax", False, "scale",
                                  "normal", intermediate=2048),
@@ -118,6 +121,8 @@ DESCRIPTIONS = {
     "skewed": "Zipf(1.2) routing: 16 ranks x 256 tokens, hidden 7168 bf16, 256 experts, top-8, max_m 256",
     "ds_prefill": "DeepSeek-shape prefill: 8 ranks x 4096 tokens, hidden 7168 fp8 e4m3 + scales, 256 experts in "
                   "8 groups, top-4 groups then top-8 of sigmoid scores, max_m 4096",
+    "mixtral_fp8": "Mixtral-shape prefill with fp8 rows: 8 ranks x 4096 tokens, hidden 4096 e4m3 + 128-elt fp32 "
+                   "scales, 8 experts, top-2 renormalised, max_m 4096",
     "ds_decode_bf16in": "DeepSeek-shape decode with bf16 input rows quantised on dispatch to fp8 e4m3 + 128-elt "
                         "fp32 scales: 8 ranks x 128 tokens, hidden 7168, 256 experts, top-8 of softmax, max_m 128",
 }
