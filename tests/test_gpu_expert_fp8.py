@@ -247,3 +247,61 @@ def test_fp8_expert_stage_rejects_bf16_rows():
         B.moe_expert_gate_up_fp8(step.desc, 256, packed.region_offsets, z, zs, z, zs, z, zs, z, zs, step.buf.err)
     assert e.value.status == B.MOE_EINVAL
     free_gpu()
+
+
+def test_fp8_expert_stage_on_the_ds_decode_shape_sampled_rows():
+    """The full DeepSeek decode shape (8 x 128 tokens, top-8 of 256 experts, H 7168,
+    I 2048, 11.3 GB of fp8 weights), checked on sampled rows of two experts: the
+    first and last row of each expert's range and one between."""
+    require_gpu()
+    w = wl.WORKLOADS["ds_decode"]
+    inp = wl.make_inputs(w)
+    ref = oracle.run(w, inp, sel=np.zeros(0, np.int64))     # layout only
+    step = P.MoeStep(w, "cuda:0")
+    d = P.to_device(inp, "cuda:0")
+    step.reset()
+    step.layout(d)
+    step.dispatch(d)
+    packed = B.allocate_packed(step.desc, "cuda:0")
+    step.recv(packed)
+    assert step.error() == B.MOE_OK
+    E, R, H, I, k, T = w.num_experts, w.num_ranks, w.hidden, w.intermediate, w.topk, w.tokens_per_rank
+    off = oracle.region_offsets(ref.counts, w.max_m)
+    assert np.array_equal(packed.region_offsets.cpu().numpy(), off)
+    rows = w.num_tokens * k
+    wts = wl.expert_weights_fp8(w, "cuda:0")
+    h = torch.empty((rows, I), dtype=torch.uint8, device="cuda:0")
+    hs = torch.empty((rows, I // 128), dtype=torch.float32, device="cuda:0")
+    y = torch.empty((rows, H), dtype=torch.bfloat16, device="cuda:0")
+    step.expert_mlp_fp8(wts, packed, h, hs, y)
+    assert step.error() == B.MOE_OK
+    ts = ref.tok_slot.astype(np.int64).reshape(-1)
+    prow = off[ts // w.max_m] + ts % w.max_m
+    owner = np.empty(rows, np.int64)
+    owner[prow] = np.arange(rows)
+    xq = inp.x.reshape(R * T, H)
+    xs = inp.x_scales.reshape(R * T, H // 128)
+    counts = off[(np.arange(E) + 1) * R] - off[np.arange(E) * R]
+    experts = [int(np.argmax(counts)), int(np.nonzero(counts)[0][0])]
+    for e in experts:
+        lo, hi = int(off[e * R]), int(off[(e + 1) * R])
+        sample = sorted({lo, hi - 1, (lo + hi) // 2})
+        q = {n: getattr(wts, n)[e].cpu().numpy() for n in ("w_gate", "w_up", "w_down")}
+        sc = {n: getattr(wts, n + "_scales")[e].cpu().numpy() for n in ("w_gate", "w_up", "w_down")}
+        Wg, Wu, Wd = (_deq_mat(q[n], sc[n]) for n in ("w_gate", "w_up", "w_down"))
+        aWg, aWu, aWd = np.abs(Wg), np.abs(Wu), np.abs(Wd)
+        for p in sample:
+            tok = owner[p] // k
+            assert inp.topk_idx.reshape(-1, k)[tok, owner[p] % k] == e
+            hv, hq_o, hs_o = oracle.gate_up_row_fp8(xq[tok], xs[tok], q["w_gate"], sc["w_gate"], q["w_up"],
+                                                    sc["w_up"])
+            eta = h_bars(_deq_row(xq[tok], xs[tok]), Wg, Wu, aWg, aWu, hv)
+            bad, tol_h = check_h_row(hv, eta, h[p].cpu().numpy(), hs[p].cpu().numpy())
+            assert bad == 0, p
+            y_o = oracle.linear_row_fp8(hq_o, hs_o, q["w_down"], sc["w_down"])
+            ty = 2.0 ** -7 * np.abs(_val(y_o)) + (I + 2) * 2.0 ** -22 * (aWd @ np.abs(_deq_row(hq_o, hs_o))) + \
+                aWd @ (2.0 * tol_h)
+            y_g = y[p].view(torch.int16).cpu().numpy().view(np.uint16)
+            assert int((np.abs(_val(y_g) - _val(y_o)) > ty).sum()) == 0, p
+    del wts, h, hs, y
+    free_gpu()
