@@ -100,15 +100,7 @@ struct GemmArgs {
 // bf16 epilogue of one 32-column chunk of a thread's accumulator row: SwiGLU
 // over gate columns g[0..31] and up columns u[0..31], or plain rounding of
 // r[0..31]; 64 bytes stored at dst.
-#ifndef MOE_GEMM_CS_STORE
-#define MOE_GEMM_CS_STORE 0
-#endif
-__device__ __forceinline__ void store16(uint4 *d, uint4 v) {
-  if (MOE_GEMM_CS_STORE)
-    __stcs(d, v);
-  else
-    *d = v;
-}
+__device__ __forceinline__ void store16(uint4 *d, uint4 v) { *d = v; }
 
 __device__ __forceinline__ void store_swiglu32(__nv_bfloat16 *dst, const uint32_t (&r)[64]) {
   uint32_t pk[16];
@@ -357,35 +349,6 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// L2 policies for TMA loads: weight tiles are kept (evict_last) while a group
-// of n-tiles sweeps the expert's rows; the rows themselves are streamed.
-#ifndef MOE_GEMM_HINT_B
-#define MOE_GEMM_HINT_B 0
-#endif
-#ifndef MOE_GEMM_HINT_A
-#define MOE_GEMM_HINT_A 0
-#endif
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                                      uint32_t bar_cluster, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
-      : "memory");
-}
-
 // TMA tile load into this CTA's shared memory, completing on an mbarrier that may
 // live in the peer CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y,
@@ -556,14 +519,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           const uint32_t sa = smem_addr(smem + s * kPairStage), fb = map_rank(smem_addr(full + s), 0);
           if (leader) mbar_arrive_expect_tx(full + s, 2 * kPairStage);
-          if (MOE_GEMM_HINT_A)
-            tma_load_2d_pair_hint(sa, &map_a, kb * kBK, arow, fb, policy_evict_first());
-          else
-            tma_load_2d_pair(sa, &map_a, kb * kBK, arow, fb);
-          if (MOE_GEMM_HINT_B)
-            tma_load_2d_pair_hint(sa + kTileA, mb, kb * kBK, brow, fb, policy_evict_last());
-          else
-            tma_load_2d_pair(sa + kTileA, mb, kb * kBK, brow, fb);
+          tma_load_2d_pair(sa, &map_a, kb * kBK, arow, fb);
+          tma_load_2d_pair(sa + kTileA, mb, kb * kBK, brow, fb);
           ++it;
         }
       }
