@@ -71,7 +71,7 @@ def _open(path: str):
     lib.moe_layout.argtypes = [pdesc] + [vp] * 6
     lib.moe_dispatch.argtypes = [pdesc] + [vp] * 9
     lib.moe_layout_dispatch.argtypes = [pdesc] + [vp] * 11
-    lib.moe_dispatch_recv.argtypes = [pdesc] + [vp] * 12
+    lib.moe_dispatch_recv.argtypes = [pdesc] + [vp] * 13
     lib.moe_combine_packed.argtypes = [pdesc] + [vp] * 7
     lib.moe_route_stats.argtypes = [pdesc, vp, ctypes.c_int32, vp, vp, vp]
     lib.moe_expert_stub.argtypes = [pdesc] + [vp] * 6
@@ -196,11 +196,12 @@ def moe_combine(desc, expert_out, topk_weights, tok_slot, flags, out, err, strea
                               _ptr(flags), _ptr(out, True), _ptr(err), _stream(stream)), "moe_combine")
 
 
-def moe_dispatch_recv(desc, counts, flags, recv_x, recv_scales, recv_meta, region_offsets, packed_x, packed_scales,
-                      packed_meta, tok_packed, err, stream=None):
+def moe_dispatch_recv(desc, counts, flags, recv_x, recv_scales, recv_meta, tok_slot, region_offsets, packed_x,
+                      packed_scales, packed_meta, tok_packed, err, stream=None):
     _check(load().moe_dispatch_recv(ctypes.byref(desc), _ptr(counts), _ptr(flags), _ptr(recv_x), _ptr(recv_scales),
-                                    _ptr(recv_meta), _ptr(region_offsets), _ptr(packed_x), _ptr(packed_scales),
-                                    _ptr(packed_meta), _ptr(tok_packed), _ptr(err), _stream(stream)),
+                                    _ptr(recv_meta), _ptr(tok_slot), _ptr(region_offsets), _ptr(packed_x),
+                                    _ptr(packed_scales), _ptr(packed_meta), _ptr(tok_packed), _ptr(err),
+                                    _stream(stream)),
            "moe_dispatch_recv")
 
 

@@ -11,6 +11,7 @@ namespace moe {
 constexpr int kMaxTopk = 16;
 constexpr int kMaxStages = 8;  // row stages of the dispatch kernels
 constexpr int kScaleBlock = 128;  // elements per fp32 scale of an fp8 row
+constexpr int kMaskedExpert = -1;  // a topk_idx entry naming no expert: skipped, no error
 
 // Limits of the bounded waits, in nanoseconds of %globaltimer. A count+1 flag
 // is published by an earlier kernel in stream order, so a zero flag means the

@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
   for (int i = tid; i < n_own; i += blockDim.x) {
     const int e = __ldg(own + i);
     if (e < 0 || e >= a.E) {
-      latch_error(a.err, MOE_EINVAL);
+      if (e != kMaskedExpert) latch_error(a.err, MOE_EINVAL);  // a masked choice is skipped silently
       continue;
     }
     const int tl = i / a.k;
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kClusterThreads) layout_cluster_kernel(LayoutA
   for (int i = tid; i < n_own; i += blockDim.x) {
     const int e = __ldg(own + i);
     if (e < 0 || e >= a.E) {
-      latch_error(a.err, MOE_EINVAL);
+      if (e != kMaskedExpert) latch_error(a.err, MOE_EINVAL);  // a masked choice is skipped silently
       continue;
     }
     const int tl = i / a.k;

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
   for (int i = tid; i < a.T * a.k; i += kFusedThreads) {
     const int e = __ldg(idx + i);
     if (e < 0 || e >= a.E) {
-      latch_error(a.err, MOE_EINVAL);
+      if (e != kMaskedExpert) latch_error(a.err, MOE_EINVAL);  // a masked choice is skipped silently
       continue;
     }
     const int t = i / a.k;

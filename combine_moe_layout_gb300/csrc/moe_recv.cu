@@ -17,7 +17,8 @@
 //                       region holding p, then the row, its scales and its
 //                       header copied with 16-byte loads and stores, and p
 //                       recorded in tok_packed[src][t][j] (the forward map the
-//                       packed combine gathers through). The grid is
+//                       packed combine gathers through; -1 for a choice with
+//                       no slot, which that warp's index p also covers). The grid is
 //                       the largest possible packed size, so the host needs no
 //                       count and the call stays asynchronous.
 #include "moe_common.cuh"
@@ -91,6 +92,7 @@ struct CompactArgs {
   const uint8_t *recv_x;
   const float *recv_scales;
   const int4 *recv_meta;
+  const int32_t *tok_slot;
   const int32_t *region_offsets;
   uint8_t *packed_x;
   float *packed_scales;
@@ -105,6 +107,10 @@ __global__ void __launch_bounds__(kCompactWarps * 32) compact_kernel(CompactArgs
   const int lane = threadIdx.x & 31;
   const int64_t p = static_cast<int64_t>(blockIdx.x) * kCompactWarps + (threadIdx.x >> 5);
   grid_dependency_wait();
+  // choice p (in [R][T][k] order) with no slot (masked, or rejected by layout)
+  // has no packed row: its forward-map entry says so. Packed rows write only
+  // the entries of choices that have a slot, so the two never meet.
+  if (lane == 0 && p < a.npacked_max && a.tok_slot[p] < 0) a.tok_packed[p] = -1;
   if (p >= a.npacked_max || p >= a.region_offsets[a.nreg]) return;
   // the region r with offsets[r] <= p < offsets[r + 1]
   int64_t lo = 0, hi = a.nreg - 1;
@@ -132,9 +138,9 @@ __global__ void __launch_bounds__(kCompactWarps * 32) compact_kernel(CompactArgs
 }
 
 moe_status launch_recv(const Sizes &s, const int32_t *counts, const uint64_t *flags, const void *recv_x,
-                       const float *recv_scales, const int32_t *recv_meta, int32_t *region_offsets, void *packed_x,
-                       float *packed_scales, int32_t *packed_meta, int32_t *tok_packed, int32_t *err,
-                       cudaStream_t stream) {
+                       const float *recv_scales, const int32_t *recv_meta, const int32_t *tok_slot,
+                       int32_t *region_offsets, void *packed_x, float *packed_scales, int32_t *packed_meta,
+                       int32_t *tok_packed, int32_t *err, cudaStream_t stream) {
   ScanArgs sa{counts, flags, region_offsets, err, static_cast<int64_t>(s.E) * s.R, s.max_m};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, 1, 1);
@@ -147,7 +153,7 @@ moe_status launch_recv(const Sizes &s, const int32_t *counts, const uint64_t *fl
   const int64_t npacked = s.ntok * s.k;
   if (npacked == 0) return MOE_OK;
   CompactArgs ca{static_cast<const uint8_t *>(recv_x), recv_scales, reinterpret_cast<const int4 *>(recv_meta),
-                 region_offsets, static_cast<uint8_t *>(packed_x), packed_scales,
+                 tok_slot, region_offsets, static_cast<uint8_t *>(packed_x), packed_scales,
                  reinterpret_cast<int4 *>(packed_meta), tok_packed, sa.nreg, npacked, s.T, s.k, s.max_m, s.nsc,
                  static_cast<uint32_t>(s.row_bytes)};
   const int64_t blocks = (npacked + kCompactWarps - 1) / kCompactWarps;
@@ -168,20 +174,22 @@ using namespace moe;
 
 extern "C" moe_status moe_dispatch_recv(const moe_desc *desc, const int32_t *counts, const uint64_t *flags,
                                         const void *recv_x, const float *recv_scales, const int32_t *recv_meta,
-                                        int32_t *region_offsets, void *packed_x, float *packed_scales,
-                                        int32_t *packed_meta, int32_t *tok_packed, int32_t *err, void *stream) {
+                                        const int32_t *tok_slot, int32_t *region_offsets, void *packed_x,
+                                        float *packed_scales, int32_t *packed_meta, int32_t *tok_packed,
+                                        int32_t *err, void *stream) {
   Sizes s;
   moe_status st = check_desc(desc, &s);
   if (st != MOE_OK) return st;
   if (counts == nullptr || flags == nullptr || region_offsets == nullptr || err == nullptr) return MOE_EINVAL;
-  if (s.ntok > 0 && (recv_x == nullptr || recv_meta == nullptr || packed_x == nullptr || packed_meta == nullptr ||
-                     tok_packed == nullptr))
+  if (s.ntok > 0 && (recv_x == nullptr || recv_meta == nullptr || tok_slot == nullptr || packed_x == nullptr ||
+                     packed_meta == nullptr || tok_packed == nullptr))
     return MOE_EINVAL;
   if (s.nsc > 0 && s.ntok > 0 && (recv_scales == nullptr || packed_scales == nullptr)) return MOE_EINVAL;
   if (!aligned16(recv_x) || !aligned16(packed_x) || !aligned16(recv_meta) || !aligned16(packed_meta) ||
       !aligned4(counts) || !aligned4(region_offsets) || !aligned4(err) || !aligned4(recv_scales) ||
-      !aligned4(packed_scales) || !aligned4(tok_packed) || (reinterpret_cast<uintptr_t>(flags) & 7u) != 0)
+      !aligned4(packed_scales) || !aligned4(tok_packed) || !aligned4(tok_slot) ||
+      (reinterpret_cast<uintptr_t>(flags) & 7u) != 0)
     return MOE_EINVAL;
-  return launch_recv(s, counts, flags, recv_x, recv_scales, recv_meta, region_offsets, packed_x, packed_scales,
-                     packed_meta, tok_packed, err, static_cast<cudaStream_t>(stream));
+  return launch_recv(s, counts, flags, recv_x, recv_scales, recv_meta, tok_slot, region_offsets, packed_x,
+                     packed_scales, packed_meta, tok_packed, err, static_cast<cudaStream_t>(stream));
 }

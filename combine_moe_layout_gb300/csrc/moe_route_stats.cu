@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kStatsThreads) route_stats_kernel(StatsArgs a)
     for (int j = 0; j < a.k; ++j) {
       const int e = __ldg(row + j);
       if (e < 0 || e >= a.E) {
-        latch_error(a.err, MOE_EINVAL);
+        if (e != kMaskedExpert) latch_error(a.err, MOE_EINVAL);  // a masked choice sends nothing
         rank[j] = -1;
         continue;
       }

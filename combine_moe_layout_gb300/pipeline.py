@@ -106,9 +106,9 @@ class MoeStep:
     def recv(self, packed: B.PackedBuffers, stream=None):
         """The receive hook: wait for the counts, pack the filled slots expert-major."""
         b = self.buf
-        B.moe_dispatch_recv(self.desc, b.counts, b.flags, b.recv_x, b.recv_scales, b.recv_meta, packed.region_offsets,
-                            packed.packed_x, packed.packed_scales, packed.packed_meta, packed.tok_packed, b.err,
-                            stream)
+        B.moe_dispatch_recv(self.desc, b.counts, b.flags, b.recv_x, b.recv_scales, b.recv_meta, b.tok_slot,
+                            packed.region_offsets, packed.packed_x, packed.packed_scales, packed.packed_meta,
+                            packed.tok_packed, b.err, stream)
 
     def combine_packed(self, d: DeviceInputs, packed_y: torch.Tensor, packed: B.PackedBuffers, stream=None,
                        out=None):

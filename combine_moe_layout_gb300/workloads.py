@@ -259,6 +259,19 @@ def make_inputs(w: Workload, seed: int | None = None) -> Inputs:
     return Inputs(idx.reshape(R, T, k), wts.reshape(R, T, k), x, sc)
 
 
+def mask_choices(inputs: Inputs, frac: float, seed: int = 1) -> Inputs:
+    """A copy of the inputs with about `frac` of the routing choices masked
+    (expert -1: the choice names no expert) and, in every rank, every choice of
+    about one token in 16 masked."""
+    rng = np.random.default_rng(seed)
+    idx = inputs.topk_idx.copy()
+    idx[rng.random(idx.shape) < frac] = -1
+    R, T, k = idx.shape
+    if T:
+        idx[:, rng.integers(0, T, size=max(1, T // 16)), :] = -1
+    return replace(inputs, topk_idx=idx)
+
+
 # --- expert weights (input generation only) ----------------------------------
 
 @dataclass

@@ -115,12 +115,14 @@ moe_status moe_buffer_sizes(const moe_desc *desc, moe_sizes *out);
  * arrived"); tok_slot[(src*T+t)*k+j] = the fixed slot of choice j of token t,
  * with pos = number of earlier tokens of src that chose the same expert (token
  * order, so positions are deterministic).
- *   topk_idx [R][T][k] int32 in [0, E), distinct within a token (read).
+ *   topk_idx [R][T][k] int32 in [0, E), distinct within a token, or -1 for a
+ *   masked choice (no expert: tok_slot = -1, nothing is sent for it and combine
+ *   takes it as a zero term; no error) (read).
  *   counts [E][R] int32, flags [E][R] uint64, tok_slot [R][T][k] int32 (written).
  *   err: device int32 error word.
- * Device errors: an expert id outside [0, E) or repeated within a token ->
- * MOE_EINVAL and tok_slot = -1 for that entry; pos >= max_m -> MOE_EOVERFLOW and
- * tok_slot = -1. */
+ * Device errors: any other expert id outside [0, E), or one repeated within a
+ * token -> MOE_EINVAL and tok_slot = -1 for that entry; pos >= max_m ->
+ * MOE_EOVERFLOW and tok_slot = -1. */
 moe_status moe_layout(const moe_desc *desc, const int32_t *topk_idx, int32_t *counts, uint64_t *flags,
                       int32_t *tok_slot, int32_t *err, void *stream);
 
@@ -169,20 +171,22 @@ int32_t moe_layout_dispatch_kernels(const moe_desc *desc);
  *   region_offsets[E*R] = total, so expert e's rows are
  *   [region_offsets[e*R], region_offsets[(e+1)*R]); slot s lands at packed row
  *   region_offsets[s / max_m] + s % max_m.
- *   counts, flags, recv_x, recv_scales, recv_meta: from layout and dispatch (read).
+ *   counts, flags, recv_x, recv_scales, recv_meta, tok_slot: from layout and
+ *   dispatch (read).
  *   region_offsets [E*R + 1] int32 (written).
  *   packed_x [R*T*k] dispatched rows, 16-byte aligned; packed_scales
  *   [R*T*k][H/128] (NULL for bf16); packed_meta [R*T*k][4] int32, 16-byte aligned
  *   (written: the first region_offsets[E*R] rows).
  *   tok_packed [R][T][k] int32 (written): the packed row of choice j of token t
- *   of rank src, the map moe_combine_packed gathers through.
+ *   of rank src, the map moe_combine_packed gathers through; -1 for a choice
+ *   with no slot (masked, or rejected by layout).
  * Device errors: a flag still zero after the bounded wait -> MOE_ETIMEOUT; a flag
  * that disagrees with its count -> MOE_EINVAL; a count above max_m ->
  * MOE_EOVERFLOW (clamped, so nothing is written out of bounds). */
 moe_status moe_dispatch_recv(const moe_desc *desc, const int32_t *counts, const uint64_t *flags, const void *recv_x,
-                             const float *recv_scales, const int32_t *recv_meta, int32_t *region_offsets,
-                             void *packed_x, float *packed_scales, int32_t *packed_meta, int32_t *tok_packed,
-                             int32_t *err, void *stream);
+                             const float *recv_scales, const int32_t *recv_meta, const int32_t *tok_slot,
+                             int32_t *region_offsets, void *packed_x, float *packed_scales, int32_t *packed_meta,
+                             int32_t *tok_packed, int32_t *err, void *stream);
 
 /* Combine reading the expert outputs in the packed layout of moe_dispatch_recv:
  * the same result as moe_combine, with choice j of token t of rank src read from
@@ -198,7 +202,8 @@ moe_status moe_combine_packed(const moe_desc *desc, const uint16_t *packed_y, co
  *   stats[src*4 + 1] = choices whose expert's rank lies on another node (one copy per expert),
  *   stats[src*4 + 2] = distinct destination ranks on other nodes, summed over tokens (per-GPU dedup),
  *   stats[src*4 + 3] = distinct destination nodes other than its own, summed over tokens (per-node dedup).
- *   topk_idx [R][T][k] (read, device or pinned host); stats [R][4] int64 (written, device).
+ *   topk_idx [R][T][k] (read, device or pinned host; -1 = a masked choice, not
+ *   counted); stats [R][4] int64 (written, device).
  * Device errors: an expert id outside [0, E) -> MOE_EINVAL (the choice is not counted). */
 moe_status moe_route_stats(const moe_desc *desc, const int32_t *topk_idx, int32_t ranks_per_node, int64_t *stats,
                            int32_t *err, void *stream);

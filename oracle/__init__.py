@@ -242,6 +242,9 @@ def dispatch(x: np.ndarray, x_scales, tok_slot: np.ndarray, num_experts: int, ma
     _check(_load().orc_dispatch(R, T, H, num_experts, k, max_m, dtype, _p(xb), _p(sc), _p(ts),
                                 sel.size, _p(sel), _p(out.slot_id), _p(out.rows), _p(out.scales),
                                 _p(out.meta)), "dispatch")
+    keep = out.slot_id >= 0                   # masked choices (-1) send nothing
+    if not keep.all():
+        out = SparseSlots(out.slot_id[keep], out.rows[keep], out.scales[keep], out.meta[keep])
     return out
 
 

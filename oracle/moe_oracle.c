@@ -222,6 +222,10 @@ int orc_layout(int R, int T, int E, int k, int max_m, const int32_t *topk_idx,
       const int32_t *row = topk_idx + ((int64_t)src * T + t) * k;
       for (int j = 0; j < k; ++j) {
         int e = row[j];
+        if (e == -1) { /* a masked choice names no expert: no slot, nothing counted */
+          tok_slot[((int64_t)src * T + t) * k + j] = -1;
+          continue;
+        }
         if (e < 0 || e >= E) return ORC_EINVAL;
         for (int jj = 0; jj < j; ++jj)
           if (row[jj] == e) return ORC_EINVAL; /* a token picks distinct experts */
@@ -280,6 +284,10 @@ int orc_dispatch(int R, int T, int H, int E, int k, int max_m, int dtype,
     }
     for (int j = 0; j < k; ++j) {
       int64_t s = tok_slot[tok * k + j];
+      if (s == -1) { /* a masked choice: nothing is sent */
+        slot_id[i * k + j] = -1;
+        continue;
+      }
       if (s < 0 || s >= nslots) {
         st = ORC_EINVAL;
         break;
@@ -456,12 +464,14 @@ int orc_route_stats(int R, int T, int E, int k, int ranks_per_node, const int32_
     for (int t = 0; t < T; ++t) {
       const int32_t *row = topk_idx + ((int64_t)src * T + t) * k;
       for (int j = 0; j < k; ++j) {
+        if (row[j] == -1) continue; /* a masked choice sends nothing */
         if (row[j] < 0 || row[j] >= E) return ORC_EINVAL;
         int rank = row[j] / L, node = rank / ranks_per_node;
         if (node == home) continue;
         per_expert += 1;
         int seen_rank = 0, seen_node = 0; /* first choice with this rank / node? */
         for (int jj = 0; jj < j; ++jj) {
+          if (row[jj] == -1) continue;
           int r2 = row[jj] / L;
           if (r2 == rank) seen_rank = 1;
           if (r2 / ranks_per_node == node) seen_node = 1;
@@ -562,6 +572,10 @@ int orc_combine(int R, int T, int H, int E, int k, int max_m, int64_t n_sel,
       break;
     }
     for (int j = 0; j < k; ++j) {
+      if (tok_slot[tok * k + j] == -1) { /* a masked choice is a zero term */
+        for (int h = 0; h < H; ++h) acc[h] = (j == 0) ? 0.0 : acc[h] + 0.0;
+        continue;
+      }
       orc_slot_ref key = {tok_slot[tok * k + j], 0};
       const orc_slot_ref *hit = (const orc_slot_ref *)bsearch(
           &key, index, (size_t)n_slots, sizeof(orc_slot_ref), orc_cmp_slot);

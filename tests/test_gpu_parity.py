@@ -16,7 +16,7 @@ from combine_moe_layout_gb300 import _binding as B
 from combine_moe_layout_gb300 import pipeline as P
 from combine_moe_layout_gb300 import workloads as wl
 from gpu_common import (TOL, assert_combine_close, check_dispatch, check_layout, check_region_sets,
-                        check_touched_slots_gpu, free_gpu, require_gpu, run_step)
+                        check_touched_slots_gpu, free_gpu, gather_slots, require_gpu, run_step)
 
 pytestmark = pytest.mark.gpu
 
@@ -285,7 +285,7 @@ def test_duplicate_expert_is_rejected_without_stray_writes(fused):
 
 
 @pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
-@pytest.mark.parametrize("bad", [8, -1, 1 << 30])
+@pytest.mark.parametrize("bad", [8, -2, 1 << 30, -(1 << 30)])
 def test_out_of_range_expert_is_rejected(bad, fused):
     w = wl.custom("oor", num_ranks=2, tokens_per_rank=8, hidden=128, num_experts=8, topk=2, max_m=8)
     idx = wl.make_inputs(w).topk_idx.copy()
@@ -491,3 +491,77 @@ def test_route_stats_reproduce_the_printed_copies_on_the_gpu(limited, key):
     assert f"{st[1] / st[0]:.2f}" == want["per_expert"]
     assert f"{st[2] / st[0]:.2f}" == want["per_gpu_dedup"]
     assert f"{st[3] / st[0]:.2f}" == want["per_node_dedup"]
+
+
+# --- masked choices (expert -1: the choice names no expert) -------------------------
+
+MASKED = {
+    # the chunk layout (T <= 128 is one chunk per rank; T = 100 here), bf16 identity experts
+    "chunk": wl.custom("masked_chunk", num_ranks=2, tokens_per_rank=100, hidden=256, num_experts=16, topk=4,
+                       max_m=100, x_dist="normal"),
+    # the cluster layout (T > 128) and, fused, the fused kernel
+    "cluster": wl.custom("masked_cluster", num_ranks=3, tokens_per_rank=700, hidden=128, num_experts=24, topk=3,
+                         max_m=700),
+    # fp8 rows with scales and the scaling experts
+    "fp8": wl.custom("masked_fp8", num_ranks=4, tokens_per_rank=64, hidden=512, num_experts=32, topk=8, max_m=64,
+                     dtype="fp8", expert="scale", x_dist="normal"),
+}
+
+
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+@pytest.mark.parametrize("name", list(MASKED))
+def test_masked_choices_are_skipped_everywhere(name, fused):
+    """About a quarter of the choices, and every choice of some tokens, are -1: no
+    error; layout, slots, combine, the receive hook and the route stats all equal
+    the oracle's, a fully masked token combines to +0, and its forward-map
+    entries read -1."""
+    require_gpu()
+    w = MASKED[name]
+    inp = wl.mask_choices(wl.make_inputs(w), 0.25)
+    ref = oracle.run(w, inp)
+    step, d, flags, err, _ = run_step(w, inp, fused=fused)
+    assert err == B.MOE_OK
+    assert np.array_equal(step.buf.counts.cpu().numpy(), ref.counts)
+    assert np.array_equal(flags.cpu().numpy().astype(np.uint64), ref.flags)
+    ts = step.buf.tok_slot.cpu().numpy()
+    assert np.array_equal(ts, ref.tok_slot)
+    assert (ts[inp.topk_idx == -1] == -1).all()
+    valid = ts.ravel() >= 0
+    rows, meta, sc = gather_slots(step, w, ts.ravel()[valid])
+    assert np.array_equal(meta, ref.slots.meta) and np.array_equal(rows, ref.slots.rows)
+    if sc is not None:
+        assert np.array_equal(sc.view(np.uint32), ref.slots.scales.view(np.uint32))
+    check_region_sets(step, w, ts, ref)
+    out = step.buf.out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert_combine_close(out.ravel(), ref.out.ravel())
+    dead = (inp.topk_idx.reshape(-1, w.topk) < 0).all(axis=1)
+    assert dead.any() and (out.reshape(-1, w.hidden)[dead] == 0).all()
+    out_slots = step.buf.out.clone()
+    # the receive hook and the packed combine (the flags were cleared by combine: signal again)
+    packed = B.allocate_packed(step.desc, "cuda:0")
+    packed.tok_packed.fill_(12345)
+    if fused:
+        step.layout_dispatch(d)
+    else:
+        step.layout(d)
+        step.dispatch(d)
+    step.recv(packed)
+    assert step.error() == B.MOE_OK
+    off = oracle.region_offsets(ref.counts, w.max_m)
+    t64 = ts.astype(np.int64)
+    want_tp = np.where(t64 >= 0, off[np.maximum(t64, 0) // w.max_m] + np.maximum(t64, 0) % w.max_m, -1)
+    assert np.array_equal(packed.tok_packed.cpu().numpy(), want_tp)
+    n = int(off[-1])
+    sop = torch.from_numpy(np.sort(t64[t64 >= 0].ravel())).cuda()   # slots in packed order
+    packed_y = step.y.index_select(0, sop).contiguous()
+    assert packed_y.shape[0] == n
+    step.combine_packed(d, packed_y, packed)
+    assert step.error() == B.MOE_OK
+    assert torch.equal(step.buf.out.view(torch.int16), out_slots.view(torch.int16))
+    # route stats
+    stats = torch.zeros((w.num_ranks, 4), dtype=torch.int64, device="cuda:0")
+    B.moe_route_stats(step.desc, d.topk_idx, 2 if w.num_ranks % 2 == 0 else 1, stats, step.buf.err)
+    assert step.error() == B.MOE_OK
+    assert np.array_equal(stats.cpu().numpy(),
+                          oracle.route_stats(inp.topk_idx, w.num_experts, 2 if w.num_ranks % 2 == 0 else 1))
+    free_gpu()

@@ -59,6 +59,11 @@ MUTANTS = [
      "int64_t sb = (int64_t)(i % 128) % (H / 128) + k / 128;"),
     ("fp8 h scale off", "float sc = amax > 0.0f ? amax / 448.0f : 1.0f;\n    hs[b] = sc;",
      "float sc = amax > 0.0f ? amax / 440.0f : 1.0f;\n    hs[b] = sc;"),
+    ("masked choice rejected", "if (e == -1) { /* a masked choice names no expert",
+     "if (e == -2) { /* a masked choice names no expert"),
+    ("masked term wipes the sum", "for (int h = 0; h < H; ++h) acc[h] = (j == 0) ? 0.0 : acc[h] + 0.0;",
+     "for (int h = 0; h < H; ++h) acc[h] = 0.0;"),
+    ("masked earlier choice read as rank 0", "if (row[jj] == -1) continue;", "if (row[jj] == -2) continue;"),
     ("quantiser scale off", "float s = amax > 0.0f ? amax / 448.0f : 1.0f;", "float s = amax > 0.0f ? amax / 447.0f : 1.0f;"),
 ]
 
@@ -88,6 +93,9 @@ PINS = [
     lambda: pins.test_linear_row_fp8_unit_scales_identity(None),
     lambda: pins.test_linear_row_fp8_matches_a_library_matmul(None),
     lambda: pins.test_gate_up_row_fp8_matches_library_ops(None),
+    lambda: pins.test_layout_with_masked_choices_matches_brute_force(None, 2, 16, 8, 2, 16, 5),
+    lambda: pins.test_combine_with_masked_choices_sums_only_the_others(None),
+    lambda: pins.test_route_stats_skip_masked_choices(None),
 ]
 
 

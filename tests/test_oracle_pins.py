@@ -173,7 +173,7 @@ def test_layout_rejects_bad_routing(oracle_lib):
     with pytest.raises(oracle.OracleError) as e:
         oracle.layout(idx, 4, 2)
     assert e.value.code == oracle.EINVAL
-    for bad in (4, -1):
+    for bad in (4, -2):   # -1 is a masked choice, not an error
         with pytest.raises(oracle.OracleError) as e:
             oracle.layout(np.array([[[0, bad]]], np.int32), 4, 2)
         assert e.value.code == oracle.EINVAL
@@ -547,3 +547,57 @@ def test_gate_up_row_fp8_matches_library_ops(oracle_lib):
     assert np.array_equal(hs, sc.numpy())
     codes = (hf / sc[:, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy().ravel()
     assert np.array_equal(hq, codes)
+
+
+# --- masked choices (expert -1) --------------------------------------------------
+
+@pytest.mark.parametrize("R,T,E,k,max_m,seed", [(2, 16, 8, 2, 16, 5), (3, 33, 16, 8, 40, 6)])
+def test_layout_with_masked_choices_matches_brute_force(oracle_lib, R, T, E, k, max_m, seed):
+    """A masked choice gets no slot and is not counted; the others keep token order."""
+    rng = np.random.default_rng(seed)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(R * T)]).astype(np.int32).reshape(R, T, k)
+    idx[rng.random(idx.shape) < 0.3] = -1
+    idx[:, 0, :] = -1                                   # a token with every choice masked
+    counts, flags, tok_slot = oracle.layout(idx, E, max_m)
+    bc, bs = _brute_layout(idx, E, max_m)
+    assert np.array_equal(counts, bc) and np.array_equal(tok_slot, bs)
+    assert (tok_slot[idx == -1] == -1).all()
+    assert counts.sum() == int((idx >= 0).sum())
+
+
+def test_combine_with_masked_choices_sums_only_the_others(oracle_lib):
+    """Identity experts: out = bf16(x * sum of the unmasked weights); a token with
+    every choice masked is exactly +0."""
+    w = wl.WORKLOADS["tiny"]
+    inp = wl.mask_choices(wl.make_inputs(w), 0.3)
+    ref = oracle.run(w, inp)
+    x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).double().numpy().reshape(-1, w.hidden)
+    wsum = np.where(inp.topk_idx >= 0, inp.topk_weights.astype(np.float64), 0.0).reshape(-1, w.topk).sum(axis=1)
+    got = torch.from_numpy(ref.out.view(np.int16)).view(torch.bfloat16).double().numpy().reshape(-1, w.hidden)
+    want = x * wsum[:, None]
+    assert (np.abs(got - want) <= np.abs(want) * 2.0 ** -8 * 1.0001).all()
+    dead = (inp.topk_idx.reshape(-1, w.topk) < 0).all(axis=1)
+    assert dead.any()
+    assert (ref.out.reshape(-1, w.hidden)[dead] == 0).all()   # +0 bits
+    # the masked choices send nothing: one slot per unmasked choice
+    assert ref.slots.slot_id.size == int((inp.topk_idx >= 0).sum())
+
+
+def test_route_stats_skip_masked_choices(oracle_lib):
+    """Counting with masked choices equals counting the same routing with those choices removed."""
+    rng = np.random.default_rng(7)
+    R, T, E, k, per_node = 8, 64, 64, 4, 2
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(R * T)]).astype(np.int32).reshape(R, T, k)
+    idx[rng.random(idx.shape) < 0.25] = -1
+    got = oracle.route_stats(idx, E, per_node)
+    L = E // R
+    want = np.zeros((R, 4), np.int64)
+    for src in range(R):
+        want[src, 0] = T
+        for t in range(T):
+            ranks = [e // L for e in idx[src, t] if e >= 0]
+            off = [r for r in ranks if r // per_node != src // per_node]
+            want[src, 1] += len(off)
+            want[src, 2] += len(set(off))
+            want[src, 3] += len({r // per_node for r in off})
+    assert np.array_equal(got, want)
