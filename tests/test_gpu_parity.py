@@ -565,3 +565,39 @@ def test_masked_choices_are_skipped_everywhere(name, fused):
     assert np.array_equal(stats.cpu().numpy(),
                           oracle.route_stats(inp.topk_idx, w.num_experts, 2 if w.num_ranks % 2 == 0 else 1))
     free_gpu()
+
+
+def test_recv_with_a_count_above_max_m_overflows_without_stray_writes():
+    """A forged count of max_m + 5 (its flag consistent with it): the receive hook
+    latches MOE_EOVERFLOW, clamps the region to max_m slots and writes nothing
+    outside its buffers; the context stays usable."""
+    require_gpu()
+    from gpu_common import Guarded
+    w = wl.custom("overflow", num_ranks=2, tokens_per_rank=16, hidden=128, num_experts=8, topk=2, max_m=16)
+    step = P.MoeStep(w, "cuda:0")
+    d = P.to_device(wl.make_inputs(w), "cuda:0")
+    step.reset()
+    step.layout(d)
+    step.dispatch(d)
+    assert step.error() == B.MOE_OK
+    r = int(torch.argmax(step.buf.counts.view(-1)).item())
+    forged = w.max_m + 5
+    step.buf.counts.view(-1)[r] = forged
+    step.buf.flags.view(-1)[r] = forged + 1
+    R, T, H, E, k = w.num_ranks, w.tokens_per_rank, w.hidden, w.num_experts, w.topk
+    n = R * T * k
+    g = {"region_offsets": Guarded((E * R + 1,), torch.int32, "cuda:0"),
+         "packed_x": Guarded((n, 2 * H), torch.uint8, "cuda:0"),
+         "packed_meta": Guarded((n, 4), torch.int32, "cuda:0"),
+         "tok_packed": Guarded((R, T, k), torch.int32, "cuda:0")}
+    packed = B.PackedBuffers(g["region_offsets"].t, g["packed_x"].t, None, g["packed_meta"].t, g["tok_packed"].t)
+    step.recv(packed)
+    assert step.error() == B.MOE_EOVERFLOW
+    assert all(v.guards_intact() for v in g.values())
+    off = packed.region_offsets.cpu().numpy()
+    assert int(off[r + 1] - off[r]) == w.max_m          # clamped
+    # the context is still usable: a clean step afterwards
+    step.reset()
+    step.run(d)
+    assert step.error() == B.MOE_OK
+    free_gpu()
