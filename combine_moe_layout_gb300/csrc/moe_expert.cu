@@ -34,11 +34,12 @@
 // A tile is up to 128 consecutive packed rows of one expert. For gate/up its
 // 256 accumulator columns are 128 gate rows i0..i0+127 of the expert's weights
 // followed by the 128 up rows of the same i, so SwiGLU pairs columns c and
-// c + 128 of a thread's own row. Tiles are numbered expert by expert; inside an
-// expert, in groups of G n-tiles, each group swept m-tile by m-tile with its G
-// n-tiles innermost. The CTAs running at one time then share both the group's
-// weight tiles and each m-tile of rows (read once per group instead of once per
-// n-tile); G balances the two (see group_width).
+// c + 128 of a thread's own row. Tiles are numbered expert by expert within two
+// classes, interleaved (see tile_of): experts with several m-tiles and experts
+// with one. Inside an expert they go in groups of G n-tiles, each group swept
+// m-tile by m-tile with its G n-tiles innermost. The CTAs running at one time
+// then share both the group's weight tiles and each m-tile of rows (read once
+// per group instead of once per n-tile); G balances the two (see group_width).
 //
 // Every wait is bounded: a timeout records MOE_ETIMEOUT, every role of the CTA
 // stops, the loads and MMAs already issued are waited for (again bounded) and
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0) tile_prefix<kBM>(offs, pref, a, lane);
   __syncthreads();
-  const int total = pref[a.E];
+  const int total = tile_total(pref, a);
   const int kblocks = a.K / kBK;
 
   if (warp == 0) {
@@ -497,7 +498,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   if (warp == 0) tile_prefix<BMP>(offs, pref, a, lane);
   cluster_sync_all();
-  const int total = *mismatch ? 0 : pref[a.E];
+  const int total = *mismatch ? 0 : tile_total(pref, a);
   const int kblocks = a.K / kBK;
   const int first = static_cast<int>(cluster_index()), stride = static_cast<int>(cluster_count());
 
@@ -627,8 +628,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
-int gemm_smem_bytes(int E) { return kSmemFixed + 8 * (E + 1); }
-int pair_smem_bytes(int E) { return kPairSmemFixed + 8 * (E + 1); }
+int gemm_smem_bytes(int E) { return kSmemFixed + 12 * (E + 1); }  // offsets + two class prefixes
+int pair_smem_bytes(int E) { return kPairSmemFixed + 12 * (E + 1); }
 
 // Whether a launch takes the CTA-pair kernel. It needs 256-row B tiles, and it
 // pays only for experts with many rows: its 256-row tiles waste half their

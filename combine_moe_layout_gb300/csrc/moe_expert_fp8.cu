@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   const uint32_t tmem_base = *tmem_slot;
   if (warp == 0) tile_prefix<kF8BM>(offs, pref, a, lane);
   __syncthreads();
-  const int total = pref[a.E];
+  const int total = tile_total(pref, a);
   const int kblocks = a.K / kF8BK;
 
   if (warp == 0) {
@@ -395,7 +395,7 @@ int fp8_group_width(const F8Args &a, int concurrent) {
 
 moe_status launch_fp8(F8Args a, const void *A, const void *B0, const void *B1, int64_t b_total_rows, int num_sms,
                       cudaStream_t stream) {
-  const int smem = kF8SmemFixed + 8 * (a.E + 1);
+  const int smem = kF8SmemFixed + 12 * (a.E + 1);  // offsets + two class prefixes
   if (smem > kF8SmemMax) return MOE_EINVAL;
   const int64_t max_tiles = (static_cast<int64_t>(a.rows) / kF8BM + a.E) * a.ntiles_n;
   if (max_tiles > INT32_MAX) return MOE_EINVAL;

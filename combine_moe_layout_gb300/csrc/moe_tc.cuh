@@ -133,15 +133,40 @@ struct Tile {
   int e, row0, rows, n0;
 };
 
-// Tile w of the CTA's sequence: its expert (pref[e] <= w < pref[e + 1]), its
-// group of group_n n-tiles (the last group may be narrower), then m-tile and,
-// innermost, the n-tile within the group.
+// The tile sequence. An expert with two or more m-tiles ("hot": its weight
+// tiles are read again from L2 by its later m-tiles) has tiles that lean on the
+// tensor cores; an expert with one m-tile ("cold") streams its weights once and
+// leans on HBM. Each class keeps its own tile prefix, pref[0..E] (hot) and
+// pref[E+1..2E+1] (cold), in expert order, and the sequence alternates a hot
+// and a cold tile for as long as both last, then runs the rest of the longer
+// class. The CTAs running at one time then keep both the tensor cores and HBM
+// busy under skewed routing; with one class empty the order is expert order.
+template <class Args>
+__device__ __forceinline__ int tile_total(const int32_t *pref, const Args &a) {
+  return pref[a.E] + pref[2 * a.E + 1];
+}
+
+// Tile w of the sequence: its class and index in the class, its expert (the
+// class prefix brackets the index), its group of group_n n-tiles (the last
+// group may be narrower), then m-tile and, innermost, the n-tile within the
+// group.
 template <int BM, class Args>
 __device__ __forceinline__ Tile tile_of(int w, const int32_t *pref, const int32_t *offs, const Args &a) {
+  const int th = pref[a.E], tc = pref[2 * a.E + 1];
+  const int both = th < tc ? th : tc;
+  int cls, idx;
+  if (w < 2 * both) {
+    cls = w & 1;
+    idx = w >> 1;
+  } else {
+    cls = th > tc ? 0 : 1;
+    idx = both + (w - 2 * both);
+  }
+  const int32_t *pc = pref + cls * (a.E + 1);
   int lo = 0, hi = a.E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (pref[mid] <= w)
+    if (pc[mid] <= idx)
       lo = mid;
     else
       hi = mid - 1;
@@ -150,7 +175,7 @@ __device__ __forceinline__ Tile tile_of(int w, const int32_t *pref, const int32_
   t.e = lo;
   const int m = offs[lo + 1] - offs[lo];
   const int mtiles = (m + BM - 1) / BM;
-  const int local = w - pref[lo];
+  const int local = idx - pc[lo];
   const int per_group = mtiles * a.group_n;
   const int g = local / per_group, r = local - g * per_group;
   const int gw = min(a.group_n, a.ntiles_n - g * a.group_n);
@@ -161,32 +186,45 @@ __device__ __forceinline__ Tile tile_of(int w, const int32_t *pref, const int32_
   return t;
 }
 
-// Tiles per expert and their prefix (one warp); an expert whose rows are not a
-// valid range of the packed buffer gets none and latches MOE_EINVAL.
+// Tiles per expert and the two class prefixes (one warp); an expert whose rows
+// are not a valid range of the packed buffer gets none and latches MOE_EINVAL.
 template <int BM, class Args>
 __device__ __forceinline__ void tile_prefix(const int32_t *offs, int32_t *pref, const Args &a, int lane) {
-  int run = 0;
+  int run_h = 0, run_c = 0;
   bool bad = false;
   for (int e0 = 0; e0 < a.E; e0 += 32) {
     const int e = e0 + lane;
-    int tiles = 0;
+    int hot = 0, cold = 0;
     if (e < a.E) {
       const int lo = offs[e], hi = offs[e + 1];
-      if (lo < 0 || hi < lo || hi > a.rows)
+      if (lo < 0 || hi < lo || hi > a.rows) {
         bad = true;
-      else
-        tiles = ((hi - lo + BM - 1) / BM) * a.ntiles_n;
+      } else {
+        const int mtiles = (hi - lo + BM - 1) / BM;
+        (mtiles >= 2 ? hot : cold) = mtiles * a.ntiles_n;
+      }
     }
-    int incl = tiles;
+    int ih = hot, ic = cold;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
+      const int vh = __shfl_up_sync(0xffffffffu, ih, o);
+      const int vc = __shfl_up_sync(0xffffffffu, ic, o);
+      if (lane >= o) {
+        ih += vh;
+        ic += vc;
+      }
     }
-    if (e < a.E) pref[e] = run + incl - tiles;
-    run += __shfl_sync(0xffffffffu, incl, 31);
+    if (e < a.E) {
+      pref[e] = run_h + ih - hot;
+      pref[a.E + 1 + e] = run_c + ic - cold;
+    }
+    run_h += __shfl_sync(0xffffffffu, ih, 31);
+    run_c += __shfl_sync(0xffffffffu, ic, 31);
   }
-  if (lane == 0) pref[a.E] = run;
+  if (lane == 0) {
+    pref[a.E] = run_h;
+    pref[2 * a.E + 1] = run_c;
+  }
   if (__any_sync(0xffffffffu, bad) && lane == 0) latch_error(a.err, MOE_EINVAL);
 }
 

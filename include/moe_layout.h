@@ -231,7 +231,7 @@ moe_status moe_expert_stub(const moe_desc *desc, const void *recv_x, const float
  *   packed_x [R*T*k][H] bf16 (read); w_gate, w_up [E][I][H] bf16 (read);
  *   h [R*T*k][I] bf16 (written for packed rows only). All four 16-byte aligned.
  * Host errors: MOE_EINVAL for another dtype, sizes or alignment, or more experts
- * than fit in shared memory (about 3900); MOE_ECUDA when no TMA tensor map can
+ * than fit in shared memory (about 2700); MOE_ECUDA when no TMA tensor map can
  * be made. Device errors: an expert whose offsets are not a range inside
  * [0, R*T*k] -> MOE_EINVAL (its rows are skipped); a stalled pipeline ->
  * MOE_ETIMEOUT. */
