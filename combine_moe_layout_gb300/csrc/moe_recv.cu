@@ -27,6 +27,7 @@ namespace moe {
 
 constexpr int kScanThreads = 1024;
 constexpr int kCompactWarps = 4;
+constexpr int kCopyBatch = 8;  // 16-byte loads in flight per lane in the row copy
 
 struct ScanArgs {
   const int32_t *counts;
@@ -126,7 +127,19 @@ __global__ void __launch_bounds__(kCompactWarps * 32) compact_kernel(CompactArgs
   const int64_t slot = lo * a.max_m + pos;
   const uint4 *src = reinterpret_cast<const uint4 *>(a.recv_x + slot * a.row_bytes);
   uint4 *dst = reinterpret_cast<uint4 *>(a.packed_x + p * a.row_bytes);
-  for (uint32_t v = lane; v < a.row_bytes / 16; v += 32) dst[v] = __ldcs(src + v);
+  // kCopyBatch loads in flight per lane before their stores: one dependent
+  // load -> store per 16 bytes would leave a warp with 512 bytes in flight,
+  // too little to cover DRAM latency with the warps an SM holds
+  const uint32_t nv = a.row_bytes / 16;
+  uint32_t v = lane;
+  for (; v + (kCopyBatch - 1) * 32 < nv; v += kCopyBatch * 32) {
+    uint4 t[kCopyBatch];
+#pragma unroll
+    for (int b = 0; b < kCopyBatch; ++b) t[b] = __ldcs(src + v + b * 32);
+#pragma unroll
+    for (int b = 0; b < kCopyBatch; ++b) dst[v + b * 32] = t[b];
+  }
+  for (; v < nv; v += 32) dst[v] = __ldcs(src + v);
   for (int c = lane; c < a.nsc; c += 32) a.packed_scales[p * a.nsc + c] = a.recv_scales[slot * a.nsc + c];
   if (lane == 0) {
     // the header {src, t, e, j} also gives combine its forward map to the packed row
