@@ -43,6 +43,10 @@ CASES = {
     # Zipf routing (hot and empty experts), three 128-wide down tiles; rows checked on a sample
     "zipf": wl.custom("fp8_zipf", num_ranks=4, tokens_per_rank=128, hidden=384, num_experts=32, topk=4,
                       max_m=128, dtype="fp8", expert="scale", router="zipf", x_dist="normal", intermediate=256),
+    # 1200 rows per expert on average (ten m-tiles each, all in the hot class, the
+    # last one ragged), three h blocks, one 256-wide down tile; rows checked on a sample
+    "many_rows": wl.custom("fp8_many", num_ranks=4, tokens_per_rank=600, hidden=256, num_experts=4, topk=2,
+                           max_m=600, dtype="fp8", expert="scale", x_dist="normal", intermediate=384),
 }
 
 
@@ -131,7 +135,7 @@ def _expert_of_rows(off, E, R, n):
 
 
 def _sample(name, n, off, E, R):
-    if name != "zipf":
+    if name not in ("zipf", "many_rows"):
         return range(n)
     firsts = {int(off[e * R]) for e in range(E) if off[(e + 1) * R] > off[e * R]}
     lasts = {int(off[(e + 1) * R]) - 1 for e in range(E) if off[(e + 1) * R] > off[e * R]}
@@ -249,12 +253,14 @@ def test_fp8_expert_stage_rejects_bf16_rows():
     free_gpu()
 
 
-def test_fp8_expert_stage_on_the_ds_decode_shape_sampled_rows():
-    """The full DeepSeek decode shape (8 x 128 tokens, top-8 of 256 experts, H 7168,
-    I 2048, 11.3 GB of fp8 weights), checked on sampled rows of two experts: the
-    first and last row of each expert's range and one between."""
+@pytest.mark.parametrize("name", ["ds_decode", "ds_prefill"])
+def test_fp8_expert_stage_on_the_deepseek_shapes_sampled_rows(name):
+    """The full DeepSeek shapes (top-8 of 256 experts, H 7168, I 2048, 11.3 GB of
+    fp8 weights): decode, 8 x 128 tokens, about 32 rows per expert; prefill,
+    8 x 4096 tokens, about 1024 rows per expert. Checked on sampled rows of two
+    experts: the first and last row of each expert's range and one between."""
     require_gpu()
-    w = wl.WORKLOADS["ds_decode"]
+    w = wl.WORKLOADS[name]
     inp = wl.make_inputs(w)
     ref = oracle.run(w, inp, sel=np.zeros(0, np.int64))     # layout only
     step = P.MoeStep(w, "cuda:0")
