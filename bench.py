@@ -422,7 +422,10 @@ def run_native(args, rank, local_rank, world):
                     "accumulate, bf16 out); synthetic experts outside the timed region",
             "l2": "flushed before every timed step, outside the timed events: a write of a buffer of 2x L2 "
                   "then a read of another (cold, clean L2)",
-            "step_kernels": "fused layout+dispatch, combine" if fused else "layout, dispatch, combine",
+            "step_kernels": (("fused layout+dispatch kernel, combine" if B.moe_layout_dispatch_kernels(step.desc) == 1
+                              else "layout+dispatch call (a layout kernel, then the dispatch kernel: the fused "
+                                   "kernel's staging does not fit this batch), combine")
+                             if fused else "layout, dispatch, combine"),
             "launch": "one CUDA graph replay per step" if args.graph else "direct launches through the C ABI",
             "receive": "receive hook packs the slots expert-major, packed combine" if packed is not None
                        else "combine reads the fixed slots",
