@@ -23,7 +23,7 @@
 // warpgroup 0 runs with 56 registers a thread and the others with 224
 // (setmaxnreg), so the promotion warps keep 128 fp32 sums in registers.
 //   warp 0      TMA producer: a 128-row x 128-byte A tile and a 256-row B tile
-//               per K block (one scale block), 128-byte swizzle, 4 stages.
+//               per K block (one scale block), 128-byte swizzle, 3 stages.
 //   warp 1      owns 512 TMEM columns (two 128 x 256 fp32 partials) and issues
 //               4 MMAs (M 128, N 256 or 128, K 32) per K block into one
 //               partial, alternating partials so the next K block's MMAs run
@@ -31,7 +31,10 @@
 //   warps 4-11  promotion and epilogue: warp w reads TMEM lanes 32 (w % 4) ..
 //               +31 (the tile's rows) and one half of the columns; it adds the
 //               scaled partial into 128 fp32 registers and, after the last K
-//               block, stores the row's part of the tile. For gate/up a warp
+//               block, stores the row's part of the tile through its own
+//               staging rows in shared memory, so that each store instruction
+//               writes whole 128-byte lines of 4 rows (64-byte pieces of 8 rows
+//               for h) rather than 16 bytes of 32 rows. For gate/up a warp
 //               holds gate and up columns of the same 64 intermediate indices,
 //               and the two warps that share a row exchange their halves of
 //               the block amax through shared memory (an mbarrier, no named
@@ -50,12 +53,23 @@ constexpr int kF8BM = 128;                      // rows of a tile
 constexpr int kF8BK = 128;                      // K per stage: one 128-byte row of e4m3, one scale block
 constexpr int kF8UK = 32;                       // K of one tcgen05.mma kind::f8f6f4
 constexpr int kF8BN = 256;                      // accumulator columns of a tile
-constexpr int kF8Stages = 4;
 constexpr int kF8TileA = kF8BM * kF8BK;         // 16 KB
 constexpr int kF8TileB = kF8BN * kF8BK;         // 32 KB
 constexpr int kF8Stage = kF8TileA + kF8TileB;
 constexpr int kF8BoxBytes = kBoxRows * kF8BK;   // one 128 x 128-byte box
 constexpr int kF8PromoWarps = 8;
+// Two forms, picked per launch (template parameters STAGES, STAGED):
+// - experts with many rows (the tensor cores bound the kernel): 3 stages and a
+//   staged epilogue. Each promotion warp writes its 32 rows of up to 128 output
+//   bytes per row into its own 4 KB of shared memory and stores them back as
+//   whole 128-byte lines (gate/up: 64-byte pieces of h), not one 16-byte piece
+//   of 32 different rows per store instruction. With two partials the MMAs run
+//   at most one K block ahead of the promotion, and a fourth stage measured no
+//   faster there; its shared memory holds the staging rows instead.
+// - experts with fewer rows than one tile (the weight stream bounds the kernel):
+//   4 stages, for the deeper weight prefetch, and direct stores of the little
+//   output there is.
+constexpr int kF8OutBytes = 4096;
 constexpr int kF8Threads = 128 + 32 * kF8PromoWarps;  // warpgroup 0: TMA, MMA (+2 idle); warpgroups 1-2: promotion
 // Register split by warpgroup (setmaxnreg): the block is launched with 168
 // registers a thread (384 threads x 168 = 64512); warpgroup 0 gives back to 56
@@ -65,9 +79,12 @@ constexpr int kF8CtrlRegs = 56;
 constexpr int kF8PromoRegs = 224;
 static_assert(128 * kF8CtrlRegs + 256 * kF8PromoRegs <= kF8Threads * kF8LaunchRegs, "register split over budget");
 constexpr uint32_t kF8TmemCols = 2 * kF8BN;     // two partials
-// stages | full, empty (S each), pfull, pempty (2 each), xbar (4), done | slot, abort | amax exchange
-constexpr int kF8Bars = 2 * kF8Stages + 2 + 2 + 4 + 1;
-constexpr int kF8SmemFixed = 1024 + kF8Stages * kF8Stage + kF8Bars * 8 + 8 + 2 * 2 * kF8BM * 4;
+// stages | epilogue staging (staged form) | full, empty (S each), pfull, pempty (2 each), xbar (4), done |
+// slot, abort | amax exchange
+__host__ __device__ constexpr int f8_smem_fixed(int stages, bool staged) {
+  return 1024 + stages * kF8Stage + (staged ? kF8PromoWarps * kF8OutBytes : 0) + (2 * stages + 2 + 2 + 4 + 1) * 8 + 8 +
+         2 * 2 * kF8BM * 4;
+}
 constexpr int kF8SmemMax = 227 * 1024;
 
 // Instruction descriptor of tcgen05.mma kind::f8f6f4: D fp32 (bits 4-5 = 1), A
@@ -141,14 +158,16 @@ __device__ __forceinline__ void mbar_arrive_local(uint64_t *bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+template <int STAGES, bool STAGED>
 __global__ void __launch_bounds__(kF8Threads, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                             const __grid_constant__ CUtensorMap map_b1, const F8Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + (((smem_addr(smem_raw) + 1023u) & ~1023u) - smem_addr(smem_raw));
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + kF8Stages * kF8Stage);
-  uint64_t *empty = full + kF8Stages;
-  uint64_t *pfull = empty + kF8Stages;
+  uint8_t *ostage = smem + STAGES * kF8Stage;  // [promotion warp][kF8OutBytes], staged form only
+  uint64_t *full = reinterpret_cast<uint64_t *>(ostage + (STAGED ? kF8PromoWarps * kF8OutBytes : 0));
+  uint64_t *empty = full + STAGES;
+  uint64_t *pfull = empty + STAGES;
   uint64_t *pempty = pfull + 2;
   uint64_t *xbar = pempty + 2;
   uint64_t *done = xbar + 4;
@@ -160,7 +179,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < kF8Stages; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
     }
@@ -204,7 +223,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         const Tile t = tile_of<kF8BM>(w, pref, offs, a);
         const int brow = t.e * a.expert_rows + t.n0;
         for (int kb = 0; kb < kblocks; ++kb) {
-          const uint32_t s = it % kF8Stages, ph = (it / kF8Stages) & 1u;
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!role_wait(empty + s, ph ^ 1u, abort, a.err)) {
             ok = false;
             break;
@@ -222,9 +241,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           ++it;
         }
       }
-      for (uint32_t s = 0; s < kF8Stages && s < it; ++s) {
-        const uint32_t last = s + ((it - 1 - s) / kF8Stages) * kF8Stages;
-        mbar_wait_bounded(full + s, (last / kF8Stages) & 1u);
+      for (uint32_t s = 0; s < STAGES && s < it; ++s) {
+        const uint32_t last = s + ((it - 1 - s) / STAGES) * STAGES;
+        mbar_wait_bounded(full + s, (last / STAGES) & 1u);
       }
     }
     __syncwarp();
@@ -237,7 +256,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       bool ok = true;
       for (int w = blockIdx.x; ok && w < total; w += gridDim.x) {
         for (int kb = 0; kb < kblocks; ++kb) {
-          const uint32_t s = it % kF8Stages, sph = (it / kF8Stages) & 1u;
+          const uint32_t s = it % STAGES, sph = (it / STAGES) & 1u;
           const uint32_t pb = pk & 1u, pph = (pk >> 1) & 1u;
           if (!role_wait(full + s, sph, abort, a.err) || !role_wait(pempty + pb, pph ^ 1u, abort, a.err)) {
             ok = false;
@@ -344,35 +363,98 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         if (!role_wait(xbar + q, static_cast<uint32_t>(lt & 1), abort, a.err)) break;
         const float amax = fmaxf(part, slot[(j ^ 1) * kF8BM + m]);
         const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-        if (valid) {
-          uint32_t pk4[16];
+        if constexpr (STAGED) {
+          // this lane's 64 codes into its staging row (64 bytes: four 16-byte pieces,
+          // piece p at p ^ ((row >> 1) & 3), so that eight rows fill all 32 banks)
+          uint4 *buf = reinterpret_cast<uint4 *>(ostage + (warp - 4) * kF8OutBytes);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint16_t lo = e4m3x2_rn_satfinite(__fdiv_rn(acc[4 * i], sc), __fdiv_rn(acc[4 * i + 1], sc));
-            const uint16_t hi = e4m3x2_rn_satfinite(__fdiv_rn(acc[4 * i + 2], sc), __fdiv_rn(acc[4 * i + 3], sc));
-            pk4[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+          for (int v = 0; v < 4; ++v) {
+            uint32_t pk4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int x = 16 * v + 4 * i;
+              const uint16_t lo = e4m3x2_rn_satfinite(__fdiv_rn(acc[x], sc), __fdiv_rn(acc[x + 1], sc));
+              const uint16_t hi = e4m3x2_rn_satfinite(__fdiv_rn(acc[x + 2], sc), __fdiv_rn(acc[x + 3], sc));
+              pk4[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+            }
+            buf[lane * 4 + (v ^ ((lane >> 1) & 3))] = make_uint4(pk4[0], pk4[1], pk4[2], pk4[3]);
           }
-          uint8_t *orow = static_cast<uint8_t *>(a.out) + arow * a.n_total + t.n0 + 64 * j;
-          uint4 *d = reinterpret_cast<uint4 *>(orow);
+          if (valid && j == 0) a.out_scales[arow * (a.n_total / 128) + t.n0 / 128] = sc;
+          __syncwarp();
+          // stores of 8 rows x 64 bytes: lane l takes piece l % 4 of row l / 4 + 8 i
+          uint8_t *obase = static_cast<uint8_t *>(a.out) + t.n0 + 64 * j;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) d[v] = make_uint4(pk4[4 * v], pk4[4 * v + 1], pk4[4 * v + 2], pk4[4 * v + 3]);
-          if (j == 0) a.out_scales[arow * (a.n_total / 128) + t.n0 / 128] = sc;
-        }
-      } else if (valid) {
-        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) + arow * a.n_total + t.n0 + cbase;
-        uint4 *d = reinterpret_cast<uint4 *>(orow);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (c < ncol) {
-            uint32_t pk2[16];
+          for (int i = 0; i < 4; ++i) {
+            const int r = (lane >> 2) + 8 * i, pc = lane & 3;
+            const uint4 v = buf[r * 4 + (pc ^ ((r >> 1) & 3))];
+            if (q * 32 + r < t.rows)
+              reinterpret_cast<uint4 *>(obase + static_cast<int64_t>(t.row0 + q * 32 + r) * a.n_total)[pc] = v;
+          }
+          __syncwarp();
+        } else {
+          if (valid) {
+            uint32_t pk4[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const __nv_bfloat162 b = __floats2bfloat162_rn(acc[32 * c + 2 * i], acc[32 * c + 2 * i + 1]);
-              pk2[i] = *reinterpret_cast<const uint32_t *>(&b);
+              const uint16_t lo = e4m3x2_rn_satfinite(__fdiv_rn(acc[4 * i], sc), __fdiv_rn(acc[4 * i + 1], sc));
+              const uint16_t hi = e4m3x2_rn_satfinite(__fdiv_rn(acc[4 * i + 2], sc), __fdiv_rn(acc[4 * i + 3], sc));
+              pk4[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
             }
+            uint8_t *orow = static_cast<uint8_t *>(a.out) + arow * a.n_total + t.n0 + 64 * j;
+            uint4 *d = reinterpret_cast<uint4 *>(orow);
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              d[4 * c + v] = make_uint4(pk2[4 * v], pk2[4 * v + 1], pk2[4 * v + 2], pk2[4 * v + 3]);
+            for (int v = 0; v < 4; ++v) d[v] = make_uint4(pk4[4 * v], pk4[4 * v + 1], pk4[4 * v + 2], pk4[4 * v + 3]);
+            if (j == 0) a.out_scales[arow * (a.n_total / 128) + t.n0 / 128] = sc;
+          }
+        }
+      } else if constexpr (STAGED) {
+        // bf16 y, 64 columns at a time: this lane's 128 bytes into its staging row
+        // (piece p at p ^ (row & 7)), then stores of 4 rows x 128 bytes, whole lines:
+        // lane l takes piece l % 8 of row l / 8 + 4 i
+        uint4 *buf = reinterpret_cast<uint4 *>(ostage + (warp - 4) * kF8OutBytes);
+        __nv_bfloat16 *obase = static_cast<__nv_bfloat16 *>(a.out) + t.n0 + cbase;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          if (2 * h2 < ncol) {
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+              uint32_t pk2[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int x = 64 * h2 + 8 * p + 2 * i;
+                const __nv_bfloat162 b = __floats2bfloat162_rn(acc[x], acc[x + 1]);
+                pk2[i] = *reinterpret_cast<const uint32_t *>(&b);
+              }
+              buf[lane * 8 + (p ^ (lane & 7))] = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = (lane >> 3) + 4 * i, p = lane & 7;
+              const uint4 v = buf[r * 8 + (p ^ (r & 7))];
+              if (q * 32 + r < t.rows)
+                reinterpret_cast<uint4 *>(obase + static_cast<int64_t>(t.row0 + q * 32 + r) * a.n_total + 64 * h2)[p] = v;
+            }
+            __syncwarp();
+          }
+        }
+      } else {
+        if (valid) {
+          __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) + arow * a.n_total + t.n0 + cbase;
+          uint4 *d = reinterpret_cast<uint4 *>(orow);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if (c < ncol) {
+              uint32_t pk2[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 b = __floats2bfloat162_rn(acc[32 * c + 2 * i], acc[32 * c + 2 * i + 1]);
+                pk2[i] = *reinterpret_cast<const uint32_t *>(&b);
+              }
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                d[4 * c + v] = make_uint4(pk2[4 * v], pk2[4 * v + 1], pk2[4 * v + 2], pk2[4 * v + 3]);
+            }
           }
         }
       }
@@ -393,10 +475,33 @@ int fp8_group_width(const F8Args &a, int concurrent) {
   return static_cast<int>(g < 1 ? 1 : (g > a.ntiles_n ? a.ntiles_n : g));
 }
 
+template <int STAGES, bool STAGED>
+moe_status launch_form(const F8Args &a, const CUtensorMap &ma, const CUtensorMap &mb0, const CUtensorMap &mb1,
+                       int64_t grid, cudaStream_t stream) {
+  auto kernel = grouped_gemm_fp8_kernel<STAGES, STAGED>;
+  const int smem = f8_smem_fixed(STAGES, STAGED) + 12 * (a.E + 1);  // offsets + two class prefixes
+  if (smem > kF8SmemMax) return MOE_EINVAL;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return MOE_ECUDA;
+  // the register split needs the launch allocation it was sized for
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess || fa.numRegs < kF8LaunchRegs) return MOE_ECUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kF8Threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  use_pdl(cfg, attr);
+  if (cudaLaunchKernelEx(&cfg, kernel, ma, mb0, mb1, a) != cudaSuccess) return MOE_ECUDA;
+  return launch_status();
+}
+
 moe_status launch_fp8(F8Args a, const void *A, const void *B0, const void *B1, int64_t b_total_rows, int num_sms,
                       cudaStream_t stream) {
-  const int smem = kF8SmemFixed + 12 * (a.E + 1);  // offsets + two class prefixes
-  if (smem > kF8SmemMax) return MOE_EINVAL;
+  // the larger of the two forms' shared memory decides which expert counts are accepted
+  if (f8_smem_fixed(4, false) + 12 * (a.E + 1) > kF8SmemMax || f8_smem_fixed(3, true) + 12 * (a.E + 1) > kF8SmemMax)
+    return MOE_EINVAL;
   const int64_t max_tiles = (static_cast<int64_t>(a.rows) / kF8BM + a.E) * a.ntiles_n;
   if (max_tiles > INT32_MAX) return MOE_EINVAL;
   const int sms = num_sms > 0 ? num_sms : sm_count();
@@ -405,24 +510,11 @@ moe_status launch_fp8(F8Args a, const void *A, const void *B0, const void *B1, i
   if (!make_map(&ma, A, a.K, a.rows, 1) || !make_map(&mb0, B0, a.K, b_total_rows, 1) ||
       !make_map(&mb1, B1, a.K, b_total_rows, 1))
     return MOE_ECUDA;
-  if (cudaFuncSetAttribute(grouped_gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-      cudaSuccess)
-    return MOE_ECUDA;
-  // the register split needs the launch allocation it was sized for
-  cudaFuncAttributes fa{};
-  if (cudaFuncGetAttributes(&fa, grouped_gemm_fp8_kernel) != cudaSuccess || fa.numRegs < kF8LaunchRegs)
-    return MOE_ECUDA;
   const int64_t grid = max_tiles < sms ? max_tiles : sms;
   if (grid <= 0) return MOE_OK;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kF8Threads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  use_pdl(cfg, attr);
-  if (cudaLaunchKernelEx(&cfg, grouped_gemm_fp8_kernel, ma, mb0, mb1, a) != cudaSuccess) return MOE_ECUDA;
-  return launch_status();
+  // fewer expected rows per expert than one tile: the weight stream bounds the launch
+  if (a.rows / a.E < kF8BM) return launch_form<4, false>(a, ma, mb0, mb1, grid, stream);
+  return launch_form<3, true>(a, ma, mb0, mb1, grid, stream);
 }
 
 moe_status check_fp8(const moe_desc *desc, int32_t inter, Sizes *s, int64_t *rows) {
