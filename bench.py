@@ -609,7 +609,11 @@ def run_expert(args, rank, local_rank, world):
     top = max(flops, key=lambda n: kern_ms[n])
     # the kernel's bound: whichever of its flops and its bytes takes longer at the measured peaks
     tensor_bound = flops[top] / (sustained * 1e12) >= gbytes[top] / (hbm * 1e9)
-    kname = "grouped_gemm_fp8_kernel" if fp8 else "grouped_gemm_kernel"
+    # the fp8 kernel's form follows the expected rows per expert: below one 128-row tile the weight stream
+    # bounds it (4 stages, direct stores), above it the tensor cores do (3 stages, staged stores)
+    rows_per_expert = w.num_tokens * w.topk // w.num_experts
+    kname = (("grouped_gemm_fp8_kernel<4, 0>" if rows_per_expert < 128 else "grouped_gemm_fp8_kernel<3, 1>")
+             if fp8 else "grouped_gemm_kernel")
     ab = dict(w.algorithmic_bytes())
     kernel_stats = {}
     for name, ms in kern_ms.items():
