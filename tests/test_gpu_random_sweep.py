@@ -1,0 +1,120 @@
+"""A seeded sweep of random small configs through the whole GPU path, against the oracle.
+
+Each case draws ranks, tokens per rank, hidden size, experts, top-k, max_m, the row
+type (bf16, fp8 with scales, bf16 quantised on dispatch), the router, masked
+choices, the dispatch form (separate calls or the fused call) and the SM count,
+within the limits the C ABI states. Every case checks, against the oracle:
+- layout: counts, count + 1 flags and slot ids exactly;
+- dispatch: each (source rank, token, choice) slot's row, scales and header bit-exact,
+  and the filled slots of every region exactly the oracle's set;
+- combine within 2^-7 relative with exact zeros (a fully masked token gives +0);
+- the receive hook: region offsets and the forward map exactly, and the packed combine
+  bit-identical to the slot combine;
+- route statistics exactly.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_moe_layout_gb300 import _binding as B
+from combine_moe_layout_gb300 import workloads as wl
+from gpu_common import assert_combine_close, check_region_sets, free_gpu, gather_slots, require_gpu, run_step
+
+pytestmark = pytest.mark.gpu
+
+# host-side checks gather every slot row: keep N * k * H (elements) bounded per case
+MAX_GATHER = 40_000_000
+
+
+def _cases(n: int = 64, seed: int = 20261202):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        R = int(rng.choice([1, 2, 3, 4, 8]))
+        E = R * int(rng.integers(1, 9))
+        k = int(rng.integers(1, min(E, 16) + 1))
+        T = int(rng.choice([1, 7, 31, 64, 100, 129, 300, 700]))
+        max_m = T + int(rng.choice([0, 0, 5, 64]))
+        dtype = str(rng.choice(["bf16", "fp8", "bf16q"]))
+        H = int(rng.choice([8, 64, 136, 512, 1032, 4096])) if dtype == "bf16" else 128 * int(rng.choice([1, 2, 3, 8, 17]))
+        if R * T * k * H > MAX_GATHER:
+            continue
+        case = dict(num_ranks=R, tokens_per_rank=T, hidden=H, num_experts=E, topk=k, max_m=max_m, dtype=dtype,
+                    router=str(rng.choice(["softmax", "zipf"])), renormalize=bool(rng.integers(0, 2)),
+                    expert="identity" if dtype == "bf16" else "scale", x_dist="normal")
+        masked = float(rng.choice([0.0, 0.0, 0.2]))
+        fused = bool(rng.integers(0, 2))
+        num_sms = int(rng.choice([0, 0, 1, 5]))
+        out.append((f"c{len(out)}", case, masked, fused, num_sms))
+    return out
+
+
+CASES = _cases()
+
+
+@pytest.mark.parametrize("name,case,masked,fused,num_sms", CASES, ids=[c[0] for c in CASES])
+def test_random_config_matches_the_oracle(name, case, masked, fused, num_sms):
+    require_gpu()
+    w = wl.custom(name, **case)
+    inp = wl.make_inputs(w, seed=int(name[1:]) + 100)
+    if masked:
+        inp = wl.mask_choices(inp, masked, seed=int(name[1:]) + 200)
+    ref = oracle.run(w, inp)
+    step, d, flags, err, _ = run_step(w, inp, num_sms=num_sms, fused=fused)
+    assert err == B.MOE_OK, B.moe_status_string(err)
+
+    # layout
+    assert np.array_equal(step.buf.counts.cpu().numpy(), ref.counts)
+    assert np.array_equal(flags.cpu().numpy().astype(np.uint64), ref.flags)
+    ts = step.buf.tok_slot.cpu().numpy()
+    assert np.array_equal(ts, ref.tok_slot)
+
+    # dispatch
+    valid = ts.ravel() >= 0
+    rows, meta, sc = gather_slots(step, w, ts.ravel()[valid])
+    assert np.array_equal(meta, ref.slots.meta) and np.array_equal(rows, ref.slots.rows)
+    if sc is not None:
+        assert np.array_equal(sc.view(np.uint32), ref.slots.scales.view(np.uint32))
+    check_region_sets(step, w, ts, ref)
+
+    # combine
+    out = step.buf.out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert_combine_close(out.ravel(), ref.out.ravel())
+    dead = (inp.topk_idx.reshape(-1, w.topk) < 0).all(axis=1)
+    if dead.any():
+        assert (out.reshape(-1, w.hidden)[dead] == 0).all()
+    assert not step.buf.flags.any().item(), "combine must clear the count+1 flags"
+    out_slots = step.buf.out.clone()
+
+    # the receive hook and the packed combine (combine cleared the flags: signal again)
+    packed = B.allocate_packed(step.desc, "cuda:0")
+    packed.tok_packed.fill_(12345)
+    if fused:
+        step.layout_dispatch(d)
+    else:
+        step.layout(d)
+        step.dispatch(d)
+    step.recv(packed)
+    assert step.error() == B.MOE_OK
+    off = oracle.region_offsets(ref.counts, w.max_m)
+    assert np.array_equal(packed.region_offsets.cpu().numpy(), off)
+    t64 = ts.astype(np.int64)
+    want_tp = np.where(t64 >= 0, off[np.maximum(t64, 0) // w.max_m] + np.maximum(t64, 0) % w.max_m, -1)
+    assert np.array_equal(packed.tok_packed.cpu().numpy(), want_tp)
+    if int(off[-1]):
+        sop = torch.from_numpy(np.sort(t64[t64 >= 0].ravel())).cuda()   # slots in packed order
+        packed_y = step.y.index_select(0, sop).contiguous()
+        step.combine_packed(d, packed_y, packed)
+        assert step.error() == B.MOE_OK
+        assert torch.equal(step.buf.out.view(torch.int16), out_slots.view(torch.int16))
+
+    # route statistics
+    rpn = 2 if w.num_ranks % 2 == 0 else 1
+    stats = torch.zeros((w.num_ranks, 4), dtype=torch.int64, device="cuda:0")
+    B.moe_route_stats(step.desc, d.topk_idx, rpn, stats, step.buf.err)
+    assert step.error() == B.MOE_OK
+    assert np.array_equal(stats.cpu().numpy(), oracle.route_stats(inp.topk_idx, w.num_experts, rpn))
+    free_gpu()
