@@ -23,7 +23,8 @@
 // warpgroup 0 runs with 56 registers a thread and the others with 224
 // (setmaxnreg), so the promotion warps keep 128 fp32 sums in registers.
 //   warp 0      TMA producer: a 128-row x 128-byte A tile and a 256-row B tile
-//               per K block (one scale block), 128-byte swizzle, 3 stages.
+//               per K block (one scale block), 128-byte swizzle, 3 or 4
+//               stages (the kernel's two forms, below).
 //   warp 1      owns 512 TMEM columns (two 128 x 256 fp32 partials) and issues
 //               4 MMAs (M 128, N 256 or 128, K 32) per K block into one
 //               partial, alternating partials so the next K block's MMAs run
@@ -31,10 +32,11 @@
 //   warps 4-11  promotion and epilogue: warp w reads TMEM lanes 32 (w % 4) ..
 //               +31 (the tile's rows) and one half of the columns; it adds the
 //               scaled partial into 128 fp32 registers and, after the last K
-//               block, stores the row's part of the tile through its own
-//               staging rows in shared memory, so that each store instruction
-//               writes whole 128-byte lines of 4 rows (64-byte pieces of 8 rows
-//               for h) rather than 16 bytes of 32 rows. For gate/up a warp
+//               block, stores the row's part of the tile: directly, or, in the
+//               form for experts of many rows, through its own staging rows in
+//               shared memory, so that each store instruction writes whole
+//               128-byte lines of 4 rows (64-byte pieces of 8 rows for h) rather
+//               than 16 bytes of 32 rows. For gate/up a warp
 //               holds gate and up columns of the same 64 intermediate indices,
 //               and the two warps that share a row exchange their halves of
 //               the block amax through shared memory (an mbarrier, no named
