@@ -285,6 +285,15 @@ def test_expert_stage_rejects_what_it_cannot_run():
     with pytest.raises(B.MoeError) as e:
         B.moe_expert_down(fp8, 2048, packed.region_offsets, h, wg, x, step.buf.err)
     assert e.value.status == B.MOE_EINVAL
+    # more experts than the kernels' shared memory holds (offsets and tile prefixes, 12 bytes per expert):
+    # rejected on the host before any tensor map or launch
+    many = B.MoeDesc(1, 4, 128, 3000, 2, 4, 0, 0)
+    off = torch.zeros(3001, dtype=torch.int32, device="cuda:0")
+    for fn in (lambda: B.moe_expert_gate_up(many, 256, off, x, wg, wg, h, step.buf.err),
+               lambda: B.moe_expert_down(many, 256, off, h, wg, x, step.buf.err)):
+        with pytest.raises(B.MoeError) as e:
+            fn()
+        assert e.value.status == B.MOE_EINVAL
     free_gpu()
 
 

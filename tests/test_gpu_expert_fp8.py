@@ -258,6 +258,14 @@ def test_fp8_expert_stage_rejects_bf16_rows():
     with pytest.raises(B.MoeError) as e:
         B.moe_expert_gate_up_fp8(step.desc, 256, packed.region_offsets, z, zs, z, zs, z, zs, z, zs, step.buf.err)
     assert e.value.status == B.MOE_EINVAL
+    # more experts than either form of the kernel holds in shared memory: rejected on the host
+    many = B.MoeDesc(1, 4, 128, 3000, 2, 4, 1, 0)
+    off = torch.zeros(3001, dtype=torch.int32, device="cuda:0")
+    for fn in (lambda: B.moe_expert_gate_up_fp8(many, 256, off, z, zs, z, zs, z, zs, z, zs, step.buf.err),
+               lambda: B.moe_expert_down_fp8(many, 256, off, z, zs, z, zs, z, step.buf.err)):
+        with pytest.raises(B.MoeError) as e:
+            fn()
+        assert e.value.status == B.MOE_EINVAL
     free_gpu()
 
 
