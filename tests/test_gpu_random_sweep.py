@@ -3,14 +3,16 @@
 Each case draws ranks, tokens per rank, hidden size, experts, top-k, max_m, the row
 type (bf16, fp8 with scales, bf16 quantised on dispatch), the router, masked
 choices, the dispatch form (separate calls or the fused call) and the SM count,
-within the limits the C ABI states. Every case checks, against the oracle:
+within the limits the C ABI states. Every step buffer sits between poisoned guard
+bands. Every case checks, against the oracle:
 - layout: counts, count + 1 flags and slot ids exactly;
 - dispatch: each (source rank, token, choice) slot's row, scales and header bit-exact,
   and the filled slots of every region exactly the oracle's set;
 - combine within 2^-7 relative with exact zeros (a fully masked token gives +0);
 - the receive hook: region offsets and the forward map exactly, and the packed combine
   bit-identical to the slot combine;
-- route statistics exactly.
+- route statistics exactly;
+- and that the guard bands are intact.
 """
 from __future__ import annotations
 
@@ -39,7 +41,8 @@ def _cases(n: int = 64, seed: int = 20261202):
         T = int(rng.choice([1, 7, 31, 64, 100, 129, 300, 700]))
         max_m = T + int(rng.choice([0, 0, 5, 64]))
         dtype = str(rng.choice(["bf16", "fp8", "bf16q"]))
-        H = int(rng.choice([8, 64, 136, 512, 1032, 4096])) if dtype == "bf16" else 128 * int(rng.choice([1, 2, 3, 8, 17]))
+        H = (int(rng.choice([8, 64, 136, 512, 1032, 4096, 7168])) if dtype == "bf16"
+             else 128 * int(rng.choice([1, 2, 3, 8, 17, 56])))
         if R * T * k * H > MAX_GATHER:
             continue
         case = dict(num_ranks=R, tokens_per_rank=T, hidden=H, num_experts=E, topk=k, max_m=max_m, dtype=dtype,
@@ -63,7 +66,7 @@ def test_random_config_matches_the_oracle(name, case, masked, fused, num_sms):
     if masked:
         inp = wl.mask_choices(inp, masked, seed=int(name[1:]) + 200)
     ref = oracle.run(w, inp)
-    step, d, flags, err, _ = run_step(w, inp, num_sms=num_sms, fused=fused)
+    step, d, flags, err, guards = run_step(w, inp, num_sms=num_sms, fused=fused, guards=True)
     assert err == B.MOE_OK, B.moe_status_string(err)
 
     # layout
@@ -117,4 +120,6 @@ def test_random_config_matches_the_oracle(name, case, masked, fused, num_sms):
     B.moe_route_stats(step.desc, d.topk_idx, rpn, stats, step.buf.err)
     assert step.error() == B.MOE_OK
     assert np.array_equal(stats.cpu().numpy(), oracle.route_stats(inp.topk_idx, w.num_experts, rpn))
+    # nothing was written outside any step buffer
+    assert all(g.guards_intact() for g in guards)
     free_gpu()
