@@ -85,3 +85,14 @@ def test_reference_arm_prints_only_on_rank_zero():
     j = json.loads(lines[0])
     assert j["impl"] == "reference" and j["n_gpus"] == 2 and j["unit"] == "tokens/s"
     assert j["cpu_baseline"]["kind"] == "oracle" and j["e2e"]["h2d_bytes_per_step"] == 0
+    # every key of the bench line's contract
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in j, key
+    assert j["steps"] == 3 and j["warmup"] == 3 and j["higher_is_better"] is True and j["scaling"] == "weak"
+    assert j["vs_baseline"] is None and j["data"] == "synthetic" and j["config"]["workload"] == "tiny"
+    assert j["value"] > 0 and j["ms_per_step"] > 0
+    for key in ("value", "unit", "cores", "kind", "sample"):
+        assert key in j["cpu_baseline"], key
+    assert j["cpu_baseline"]["value"] == j["value"] and j["cpu_baseline"]["cores"] >= 1
+    assert j["e2e"]["value"] == j["value"] and j["e2e"]["unit"] == j["unit"] and j["e2e"]["d2h_bytes_per_step"] == 0
