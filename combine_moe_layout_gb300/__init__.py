@@ -8,8 +8,8 @@ seeded workload generators.
 from ._binding import (  # noqa: F401
     MOE_BF16,
     MOE_BF16_TO_FP8,
-    MOE_EINVAL,
     MOE_ECUDA,
+    MOE_EINVAL,
     MOE_ENOMEM,
     MOE_EOVERFLOW,
     MOE_ETIMEOUT,
@@ -28,6 +28,11 @@ from ._binding import (  # noqa: F401
     moe_combine_packed,
     moe_dispatch,
     moe_dispatch_recv,
+    moe_expert_down,
+    moe_expert_down_fp8,
+    moe_expert_gate_up,
+    moe_expert_gate_up_fp8,
+    moe_expert_mlp_noalloc,
     moe_expert_stub,
     moe_get_error,
     moe_layout,
