@@ -37,6 +37,14 @@ def test_library_exports_every_declared_symbol():
         assert set(declared_functions()) <= exported
 
 
+def test_every_declared_entry_point_has_a_python_name():
+    """The binding calls each C entry point by its own name, and the package exports it."""
+    import combine_moe_layout_gb300 as pkg
+    for name in declared_functions():
+        assert callable(getattr(B, name, None)), f"{name} has no binding"
+        assert getattr(pkg, name, None) is getattr(B, name), f"{name} is not exported by the package"
+
+
 def test_library_is_built_for_sm_103a():
     assert "arch=compute_103a,code=sm_103a" in " ".join(_build.ARCH)
 
