@@ -697,7 +697,9 @@ int group_width(const GemmArgs &a, int concurrent, int tile_rows) {
 moe_status launch_grouped(GemmArgs a, const void *A, const void *B0, const void *B1, int64_t b_total_rows,
                           int num_sms, cudaStream_t stream) {
   const int sms_all = num_sms > 0 ? num_sms : sm_count();
-  a.group_n = use_pair(a) ? group_width(a, sms_all / 2, 2 * kBM) : group_width(a, sms_all, kBM);
+  // a CTA pair needs two SMs: with one, the one-CTA kernel runs every launch
+  const bool pair = use_pair(a) && sms_all >= 2;
+  a.group_n = pair ? group_width(a, sms_all / 2, 2 * kBM) : group_width(a, sms_all, kBM);
   const int smem = gemm_smem_bytes(a.E);
   if (smem > kSmemMax) return MOE_EINVAL;
   const int64_t max_tiles = (static_cast<int64_t>(a.rows) / kBM + a.E) * a.ntiles_n;
@@ -706,7 +708,7 @@ moe_status launch_grouped(GemmArgs a, const void *A, const void *B0, const void 
   if (!make_map(&ma, A, a.K, a.rows) || !make_map(&mb0, B0, a.K, b_total_rows) ||
       !make_map(&mb1, B1, a.K, b_total_rows))
     return MOE_ECUDA;
-  if (use_pair(a)) return launch_pair(a, ma, mb0, mb1, num_sms, stream);
+  if (pair) return launch_pair(a, ma, mb0, mb1, num_sms, stream);
   if (cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return MOE_ECUDA;
   const int sms = num_sms > 0 ? num_sms : sm_count();
