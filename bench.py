@@ -25,6 +25,7 @@ the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import os
@@ -713,18 +714,19 @@ def cpu_baseline_expert(w, inp, seconds: float) -> dict:
             oracle.linear_row_fp8(hq, hs, wd, sd)
         weights = "random e4m3 weight codes (the oracle's cost does not depend on them)"
     spent, n = 0.0, 0
-    while n < 1 or spent < seconds:
-        tok = (n * 7919) % w.num_tokens
-        t0 = time.perf_counter()
-        for e in idx[tok]:
-            row(tok, e)
-        spent += time.perf_counter() - t0
-        n += 1
+    with _one_core() as core:
+        while n < 1 or spent < seconds:
+            tok = (n * 7919) % w.num_tokens
+            t0 = time.perf_counter()
+            for e in idx[tok]:
+                row(tok, e)
+            spent += time.perf_counter() - t0
+            n += 1
     per_tok = spent / n + t_layout / w.num_tokens
     return {"value": round(1.0 / per_tok, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"layout of all {w.num_tokens} tokens + the {w.topk} expert MLP rows of {n} tokens, "
                       f"single-threaded C oracle (fp64), {weights}", "seconds": round(spent + t_layout, 2),
-            "cpu": _cpu_model()}
+            "cpu": _cpu_model(), "pinned_core": core}
 
 
 # --- the CPU oracle (baseline leg and reference arm) ---------------------------------
@@ -746,6 +748,24 @@ def _oracle_sample_step(w, inp, sel):
     return (t1 - t0) + (t3 - t2)
 
 
+@contextlib.contextmanager
+def _one_core():
+    """Pin the calling thread (the one that runs the single-threaded oracle) to one
+    core while the oracle is timed, and restore its affinity afterwards; yields the
+    core, or None where affinity cannot be set."""
+    try:
+        old = os.sched_getaffinity(0)
+        core = min(old)
+        os.sched_setaffinity(0, {core})
+    except (AttributeError, OSError, ValueError):
+        yield None
+        return
+    try:
+        yield core
+    finally:
+        os.sched_setaffinity(0, old)
+
+
 def _cpu_model():
     try:
         for line in open("/proc/cpuinfo"):
@@ -761,15 +781,16 @@ def cpu_baseline(w, inp, seconds: float) -> dict:
     import numpy as np
     sel = np.arange(w.num_tokens, dtype=np.int64)
     spent, reps = 0.0, 0
-    while reps < 1 or spent < seconds:
-        spent += _oracle_sample_step(w, inp, sel)
-        reps += 1
-        if reps >= 50:
-            break
+    with _one_core() as core:
+        while reps < 1 or spent < seconds:
+            spent += _oracle_sample_step(w, inp, sel)
+            reps += 1
+            if reps >= 50:
+                break
     return {"value": round(reps * w.num_tokens / spent, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{reps} full {w.name} steps ({w.num_tokens} tokens each), single-threaded C oracle "
                       f"(gcc -O2), synthetic experts excluded", "seconds": round(spent, 2),
-            "cpu": _cpu_model(), "host_cores_available": os.cpu_count()}
+            "cpu": _cpu_model(), "host_cores_available": os.cpu_count(), "pinned_core": core}
 
 
 def run_reference(args, rank, local_rank, world):
@@ -794,9 +815,10 @@ def run_reference(args, rank, local_rank, world):
         cursor = (cursor + n) % w.num_tokens
         return s
 
-    for _ in range(W):
-        _oracle_sample_step(w, inp, next_sel())
-    spent = sum(_oracle_sample_step(w, inp, next_sel()) for _ in range(K))
+    with _one_core() as core:
+        for _ in range(W):
+            _oracle_sample_step(w, inp, next_sel())
+        spent = sum(_oracle_sample_step(w, inp, next_sel()) for _ in range(K))
     value = K * n / spent
     return {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
@@ -805,7 +827,7 @@ def run_reference(args, rank, local_rank, world):
         "config": {"workload": w.name, "description": wl.DESCRIPTIONS[w.name],
                    "sample": f"{n} of {w.num_tokens} tokens per step (layout over all tokens)"},
         "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{n} tokens per step, {K} steps", "cpu": _cpu_model()},
+                         "sample": f"{n} tokens per step, {K} steps", "cpu": _cpu_model(), "pinned_core": core},
         "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
