@@ -115,6 +115,30 @@ def test_algorithmic_bytes_of_the_decode_step():
     assert 195e6 < b["total"] < 205e6
 
 
+# The per-config algorithmic bytes the step is measured against (MB): layout (bytes), dispatch, combine, total.
+# Those count a 4-byte source-token index per slot; the dispatch here writes a 16-byte header {src, t, e, j} per
+# slot instead, so its dispatch bytes are 12 bytes per dispatched choice above them.
+CONTRACT_BYTES = {
+    "tiny": (704, 0.025, 0.025, 0.051),
+    "ds_decode": (90112, 68.19, 132.19, 200.47),
+    "mixtral": (525056, 805.83, 805.83, 1612.19),
+    "skewed": (311296, 528.74, 528.74, 1057.80),
+    "ds_prefill": (2121728, 2182.09, 4229.96, 6414.16),
+}
+
+
+@pytest.mark.parametrize("name", list(CONTRACT_BYTES))
+def test_algorithmic_bytes_match_the_contract(name):
+    w = wl.WORKLOADS[name]
+    b = w.algorithmic_bytes()
+    lay, dis, com, tot = CONTRACT_BYTES[name]
+    header_extra = w.num_tokens * w.topk * 12
+    assert b["layout"] == lay
+    assert abs(b["combine"] / 1e6 - com) < 0.006
+    assert abs((b["dispatch"] - header_extra) / 1e6 - dis) < 0.006
+    assert abs((b["total"] - header_extra) / 1e6 - tot) < 0.006
+
+
 def _page_routing(limited: bool):
     """The page's simulation as a routing of 64 ranks (8 nodes of 8): rank 0 holds the page's 4096 tokens."""
     g = json.load(open(os.path.join(GOLDEN, "node_limited_routing.json")))["setup"]
