@@ -326,9 +326,63 @@ def run_native(args, rank, local_rank, world):
         out_view = step.buf.out.view(w.num_tokens, w.hidden)
         eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         mode = args.e2e_mode
-        if mode == "auto":   # small batches: the copy engine brings the inputs in faster than the kernels pull them
-            mode = "hybrid" if w.num_tokens <= 2048 else "zero-copy"
-        if mode == "copy":
+        if mode == "auto":
+            # small batches: the copy engine brings the inputs in faster than the kernels pull them, and the
+            # next step's copy overlaps this step; large ones: the kernels read the inputs straight from host memory
+            mode = "pipelined" if w.num_tokens <= 2048 else "zero-copy"
+        if mode == "pipelined" and (packed is not None or
+                                    2 * sum(B.moe_buffer_sizes(step.desc).values()) > torch.cuda.mem_get_info(dev)[0] // 2):
+            mode = "hybrid"   # the packed path, or no room for two more sets of step buffers
+        e2e_ms = None
+        if mode == "pipelined":
+            # consecutive steps overlap: step i + 1's inputs are copied in on a second stream while step i
+            # dispatches and combines (combine writing the bf16 output into pinned host memory). Three sets of
+            # step buffers rotate, so the expert outputs a step reads were last touched two steps (about twice
+            # a step's traffic, several times L2) earlier; no L2 flush sits between the steps.
+            ring = [step] + [P.MoeStep(w, dev, args.num_sms) for _ in range(2)]
+            for r_ in ring[1:]:
+                r_.reset()
+                r_.run(d)  # the synthetic experts once, as for the first set
+            dpacks = [dpack, torch.empty_like(dpack)]
+            d2s = [inputs_in(p_) for p_ in dpacks]
+            hout_steps = hout.view(w.num_ranks, w.tokens_per_rank, w.hidden)
+            copy_stream = torch.cuda.Stream(dev)
+
+            def pipelined(n):
+                copied = [torch.cuda.Event() for _ in range(n)]
+                read = [torch.cuda.Event() for _ in range(n)]
+                for i in range(n):
+                    with torch.cuda.stream(copy_stream):
+                        if i >= 2:
+                            copy_stream.wait_event(read[i - 2])  # step i - 2's dispatch has read this pack
+                        dpacks[i % 2].copy_(hpack, non_blocking=True)
+                        copied[i].record(copy_stream)
+                    stream.wait_event(copied[i])
+                    r_ = ring[i % 3]
+                    if fused:
+                        r_.layout_dispatch(d2s[i % 2])
+                    else:
+                        r_.layout(d2s[i % 2])
+                        r_.dispatch(d2s[i % 2])
+                    read[i].record(stream)
+                    r_.combine(d2s[i % 2], out=hout_steps)
+                stream.wait_stream(copy_stream)
+
+            pipelined(W)
+            torch.cuda.synchronize()
+            t0_, t1_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0_.record(stream)
+            pipelined(K)
+            t1_.record(stream)
+            torch.cuda.synchronize()
+            e2e_ms = t0_.elapsed_time(t1_)
+            for r_ in ring:
+                if r_.error() != B.MOE_OK:
+                    raise RuntimeError("pipelined end-to-end steps latched an error")
+            how = ("pipelined: each step's packed inputs copied in by a copy engine on a second stream while the "
+                   "previous step dispatches and combines; combine writes the bf16 output straight into pinned host "
+                   "memory; three sets of step buffers rotate instead of an L2 flush between steps")
+        elif mode == "copy":
             d2 = inputs_in(dpack)
             for i in range(K):
                 flush()
@@ -360,7 +414,8 @@ def run_native(args, rank, local_rank, world):
             how = ("zero-copy: the kernels read the packed inputs from pinned host memory and write the bf16 "
                    "output into pinned host memory over NVLink-C2C, no separate copies")
         torch.cuda.synchronize()
-        e2e_ms = sum(a.elapsed_time(b) for a, b in eev)
+        if e2e_ms is None:
+            e2e_ms = sum(a.elapsed_time(b) for a, b in eev)
         e2e = {"value": None, "unit": "tokens/s", "h2d_bytes_per_step": int(sum(a_.size for a_ in parts)),
                "d2h_bytes_per_step": hout.numel() * 2, "local_ms_total": e2e_ms, "mode": mode, "copies": how}
         if mode != "copy":
@@ -901,11 +956,12 @@ def main(argv=None):
     ap.add_argument("--calibrate", action="store_true",
                     help="print the bandwidth of plain device writes and copies at the step's sizes and exit")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-mode", choices=("auto", "hybrid", "zero-copy", "copy"), default="auto",
-                    help="end to end: auto = hybrid up to 2048 tokens, zero-copy above; "
+    ap.add_argument("--e2e-mode", choices=("auto", "hybrid", "zero-copy", "copy", "pipelined"), default="auto",
+                    help="end to end: auto = pipelined up to 2048 tokens, zero-copy above; "
                          "hybrid = a copy engine moves the inputs in and combine writes the output "
                          "straight to pinned host memory; zero-copy = the kernels also read the inputs from host "
-                         "memory; copy = copy engines move both")
+                         "memory; copy = copy engines move both; pipelined = hybrid with each step's input copy "
+                         "overlapping the previous step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)
