@@ -33,6 +33,7 @@ from ._binding import (  # noqa: F401
     moe_expert_gate_up,
     moe_expert_gate_up_fp8,
     moe_expert_mlp_noalloc,
+    moe_expert_mlp_noalloc_fp8,
     moe_expert_stub,
     moe_get_error,
     moe_layout,

@@ -78,6 +78,7 @@ def _open(path: str):
     lib.moe_expert_gate_up.argtypes = [pdesc, ctypes.c_int32] + [vp] * 7
     lib.moe_expert_down.argtypes = [pdesc, ctypes.c_int32] + [vp] * 6
     lib.moe_expert_mlp_noalloc.argtypes = [pdesc, ctypes.c_int32] + [vp] * 8
+    lib.moe_expert_mlp_noalloc_fp8.argtypes = [pdesc, ctypes.c_int32] + [vp] * 12
     lib.moe_expert_gate_up_fp8.argtypes = [pdesc, ctypes.c_int32] + [vp] * 11
     lib.moe_expert_down_fp8.argtypes = [pdesc, ctypes.c_int32] + [vp] * 8
     lib.moe_combine.argtypes = [pdesc] + [vp] * 7
@@ -90,7 +91,7 @@ def _open(path: str):
     for name in ("moe_buffer_sizes", "moe_layout", "moe_dispatch", "moe_layout_dispatch", "moe_dispatch_recv",
                  "moe_expert_stub", "moe_combine", "moe_combine_packed", "moe_route_stats", "moe_reset",
                  "moe_expert_gate_up", "moe_expert_down", "moe_expert_mlp_noalloc", "moe_expert_gate_up_fp8",
-                 "moe_expert_down_fp8",
+                 "moe_expert_down_fp8", "moe_expert_mlp_noalloc_fp8",
                  "moe_get_error"):
         getattr(lib, name).restype = st
     return lib
@@ -189,6 +190,14 @@ def moe_expert_mlp_noalloc(desc, inter: int, region_offsets, packed_x, w_gate, w
     _check(load().moe_expert_mlp_noalloc(ctypes.byref(desc), int(inter), _ptr(region_offsets), _ptr(packed_x),
                                          _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(packed_y), _ptr(err),
                                          _stream(stream)), "moe_expert_mlp_noalloc")
+
+
+def moe_expert_mlp_noalloc_fp8(desc, inter: int, region_offsets, packed_x, packed_scales, w_gate, w_gate_scales,
+                               w_up, w_up_scales, w_down, w_down_scales, packed_y, err, stream=None):
+    _check(load().moe_expert_mlp_noalloc_fp8(ctypes.byref(desc), int(inter), _ptr(region_offsets), _ptr(packed_x),
+                                             _ptr(packed_scales), _ptr(w_gate), _ptr(w_gate_scales), _ptr(w_up),
+                                             _ptr(w_up_scales), _ptr(w_down), _ptr(w_down_scales), _ptr(packed_y),
+                                             _ptr(err), _stream(stream)), "moe_expert_mlp_noalloc_fp8")
 
 
 def moe_combine(desc, expert_out, topk_weights, tok_slot, flags, out, err, stream=None):

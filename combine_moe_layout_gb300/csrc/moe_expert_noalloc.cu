@@ -51,3 +51,29 @@ extern "C" moe_status moe_expert_mlp_noalloc(const moe_desc *desc, int32_t inter
   if (a != MOE_OK) return a;
   return moe_expert_down(desc, inter, region_offsets, h, w_down, packed_y, err, stream);
 }
+
+// The fp8 expert stage in one call that allocates nothing: h (e4m3, R*T*k x I
+// bytes) at the start of the same scratch and its 128-element scales after it,
+// at the next 256-byte boundary. The same race rule applies.
+extern "C" moe_status moe_expert_mlp_noalloc_fp8(const moe_desc *desc, int32_t inter, const int32_t *region_offsets,
+                                                 const void *packed_x, const float *packed_scales, const void *w_gate,
+                                                 const float *w_gate_scales, const void *w_up,
+                                                 const float *w_up_scales, const void *w_down,
+                                                 const float *w_down_scales, void *packed_y, int32_t *err,
+                                                 void *stream) {
+  moe::Sizes s;
+  const moe_status st = moe::check_desc(desc, &s);
+  if (st != MOE_OK) return st;
+  if (inter < 128 || inter % 128 != 0) return MOE_EINVAL;
+  const uint64_t rows = static_cast<uint64_t>(s.ntok) * static_cast<uint64_t>(s.k);
+  const uint64_t h_bytes = (rows * static_cast<uint64_t>(inter) + 255u) & ~uint64_t(255);
+  const uint64_t sc_bytes = rows * static_cast<uint64_t>(inter / 128) * 4u;
+  if (h_bytes + sc_bytes > kScratchBytes) return MOE_ENOMEM;
+  uint8_t *h = static_cast<uint8_t *>(scratch_address());
+  if (h == nullptr) return MOE_ECUDA;
+  float *h_scales = reinterpret_cast<float *>(h + h_bytes);
+  const moe_status a = moe_expert_gate_up_fp8(desc, inter, region_offsets, packed_x, packed_scales, w_gate,
+                                              w_gate_scales, w_up, w_up_scales, h, h_scales, err, stream);
+  if (a != MOE_OK) return a;
+  return moe_expert_down_fp8(desc, inter, region_offsets, h, h_scales, w_down, w_down_scales, packed_y, err, stream);
+}

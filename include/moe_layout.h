@@ -294,6 +294,19 @@ moe_status moe_expert_mlp_noalloc(const moe_desc *desc, int32_t inter, const int
                                   const void *packed_x, const void *w_gate, const void *w_up, const void *w_down,
                                   void *packed_y, int32_t *err, void *stream);
 
+/* The fp8 expert stage (moe_expert_gate_up_fp8 then moe_expert_down_fp8) in one
+ * call that allocates nothing, like moe_expert_mlp_noalloc and in the same fixed
+ * array: h (R*T*k * inter e4m3 bytes, rounded up to 256) and then its scales
+ * (R*T*k * inter/128 floats) may not exceed 32 MiB together (MOE_ENOMEM
+ * otherwise, nothing launched). The same race rule applies. Arguments, results
+ * and other errors as moe_expert_gate_up_fp8 and moe_expert_down_fp8 (inter a
+ * multiple of 128); MOE_ECUDA if the array's address cannot be obtained. */
+moe_status moe_expert_mlp_noalloc_fp8(const moe_desc *desc, int32_t inter, const int32_t *region_offsets,
+                                      const void *packed_x, const float *packed_scales, const void *w_gate,
+                                      const float *w_gate_scales, const void *w_up, const float *w_up_scales,
+                                      const void *w_down, const float *w_down_scales, void *packed_y, int32_t *err,
+                                      void *stream);
+
 /* Combine (Perplexity, "Combine"; "How GPUs Talk", section 7). For every token:
  * out[src][t][h] = bf16_rne( sum_{j<k} w[src][t][j] * Y[tok_slot[src][t][j]][h] ),
  * the products and sum in fp32, choices in order j = 0..k-1, weights applied at
