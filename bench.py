@@ -335,38 +335,53 @@ def run_native(args, rank, local_rank, world):
             mode = "hybrid"   # the packed path, or no room for two more sets of step buffers
         e2e_ms = None
         if mode == "pipelined":
-            # consecutive steps overlap: step i + 1's inputs are copied in on a second stream while step i
-            # dispatches and combines (combine writing the bf16 output into pinned host memory). Three sets of
-            # step buffers rotate, so the expert outputs a step reads were last touched two steps (about twice
-            # a step's traffic, several times L2) earlier; no L2 flush sits between the steps.
+            # consecutive steps overlap on three streams: step i + 1's inputs are copied in by a copy engine
+            # while step i + 1 dispatches (a high-priority stream, so its blocks take SM slots as step i's
+            # combine blocks retire) beside step i's combine, which writes the bf16 output into pinned host
+            # memory over NVLink-C2C. Three sets of step buffers, input packs and host outputs rotate: set
+            # i % 3 is reused by step i + 3 once step i's combine (the last reader of its pack, slot ids and
+            # flags) is done. The expert outputs a step reads were last touched two steps (about twice a
+            # step's traffic, several times L2) earlier, so no L2 flush sits between the steps.
             ring = [step] + [P.MoeStep(w, dev, args.num_sms) for _ in range(2)]
             for r_ in ring[1:]:
                 r_.reset()
                 r_.run(d)  # the synthetic experts once, as for the first set
-            dpacks = [dpack, torch.empty_like(dpack)]
+            dpacks = [dpack] + [torch.empty_like(dpack) for _ in range(2)]
             d2s = [inputs_in(p_) for p_ in dpacks]
-            hout_steps = hout.view(w.num_ranks, w.tokens_per_rank, w.hidden)
+            houts = [hout] + [torch.empty_like(hout).pin_memory() for _ in range(2)]
+            hout_steps = [h_.view(w.num_ranks, w.tokens_per_rank, w.hidden) for h_ in houts]
             copy_stream = torch.cuda.Stream(dev)
+            disp_stream = torch.cuda.Stream(dev, priority=-1)  # a lower number is a higher priority
+            comb_stream = torch.cuda.Stream(dev, priority=0)
+            side = (copy_stream, disp_stream, comb_stream)
 
             def pipelined(n):
+                for s_ in side:
+                    s_.wait_stream(stream)
                 copied = [torch.cuda.Event() for _ in range(n)]
-                read = [torch.cuda.Event() for _ in range(n)]
+                dispatched = [torch.cuda.Event() for _ in range(n)]
+                done = [torch.cuda.Event() for _ in range(n)]
                 for i in range(n):
+                    j = i % 3
+                    if i >= 3:
+                        copy_stream.wait_event(done[i - 3])  # step i - 3 no longer reads set j
                     with torch.cuda.stream(copy_stream):
-                        if i >= 2:
-                            copy_stream.wait_event(read[i - 2])  # step i - 2's dispatch has read this pack
-                        dpacks[i % 2].copy_(hpack, non_blocking=True)
+                        dpacks[j].copy_(hpack, non_blocking=True)
                         copied[i].record(copy_stream)
-                    stream.wait_event(copied[i])
-                    r_ = ring[i % 3]
-                    if fused:
-                        r_.layout_dispatch(d2s[i % 2])
-                    else:
-                        r_.layout(d2s[i % 2])
-                        r_.dispatch(d2s[i % 2])
-                    read[i].record(stream)
-                    r_.combine(d2s[i % 2], out=hout_steps)
-                stream.wait_stream(copy_stream)
+                    disp_stream.wait_event(copied[i])
+                    with torch.cuda.stream(disp_stream):
+                        if fused:
+                            ring[j].layout_dispatch(d2s[j])
+                        else:
+                            ring[j].layout(d2s[j])
+                            ring[j].dispatch(d2s[j])
+                        dispatched[i].record(disp_stream)
+                    comb_stream.wait_event(dispatched[i])
+                    with torch.cuda.stream(comb_stream):
+                        ring[j].combine(d2s[j], out=hout_steps[j])
+                        done[i].record(comb_stream)
+                for s_ in side:
+                    stream.wait_stream(s_)
 
             pipelined(W)
             torch.cuda.synchronize()
@@ -379,9 +394,10 @@ def run_native(args, rank, local_rank, world):
             for r_ in ring:
                 if r_.error() != B.MOE_OK:
                     raise RuntimeError("pipelined end-to-end steps latched an error")
-            how = ("pipelined: each step's packed inputs copied in by a copy engine on a second stream while the "
-                   "previous step dispatches and combines; combine writes the bf16 output straight into pinned host "
-                   "memory; three sets of step buffers rotate instead of an L2 flush between steps")
+            how = ("pipelined: each step's packed inputs copied in by a copy engine on its own stream; the step "
+                   "dispatches on a high-priority stream beside the previous step's combine, which writes the bf16 "
+                   "output straight into pinned host memory; three sets of step buffers, input packs and host "
+                   "outputs rotate instead of an L2 flush between steps")
         elif mode == "copy":
             d2 = inputs_in(dpack)
             for i in range(K):
@@ -421,8 +437,10 @@ def run_native(args, rank, local_rank, world):
         if mode != "copy":
             path(d)  # the same step on device buffers, to compare
             torch.cuda.synchronize()
-        if not torch.equal(hout.view(torch.int16), out_view.cpu().view(torch.int16)):
-            raise RuntimeError("end-to-end output differs from the device output")
+        want = out_view.cpu().view(torch.int16)
+        for h_ in (houts if mode == "pipelined" else [hout]):
+            if not torch.equal(h_.view(torch.int16), want):
+                raise RuntimeError("end-to-end output differs from the device output")
 
     clocks = sampler.stop()
     status = step.error()
