@@ -330,18 +330,21 @@ def run_native(args, rank, local_rank, world):
             # small batches: the copy engine brings the inputs in faster than the kernels pull them, and the
             # next step's copy overlaps this step; large ones: the kernels read the inputs straight from host memory
             mode = "pipelined" if w.num_tokens <= 2048 else "zero-copy"
-        if mode == "pipelined" and (packed is not None or
+        if mode.startswith("pipelined") and (packed is not None or
                                     2 * sum(B.moe_buffer_sizes(step.desc).values()) > torch.cuda.mem_get_info(dev)[0] // 2):
             mode = "hybrid"   # the packed path, or no room for two more sets of step buffers
         e2e_ms = None
-        if mode == "pipelined":
-            # consecutive steps overlap on three streams: step i + 1's inputs are copied in by a copy engine
+        if mode in ("pipelined", "pipelined-copy"):
+            # consecutive steps overlap on several streams: step i + 1's inputs are copied in by a copy engine
             # while step i + 1 dispatches (a high-priority stream, so its blocks take SM slots as step i's
-            # combine blocks retire) beside step i's combine, which writes the bf16 output into pinned host
-            # memory over NVLink-C2C. Three sets of step buffers, input packs and host outputs rotate: set
-            # i % 3 is reused by step i + 3 once step i's combine (the last reader of its pack, slot ids and
-            # flags) is done. The expert outputs a step reads were last touched two steps (about twice a
-            # step's traffic, several times L2) earlier, so no L2 flush sits between the steps.
+            # combine blocks retire) beside step i's combine. "pipelined": combine writes the bf16 output into
+            # pinned host memory over NVLink-C2C. "pipelined-copy": combine writes it to device memory and a
+            # second copy engine, on a fourth stream, moves it to pinned host memory while the SMs go on with
+            # the next step. Three sets of step buffers, input packs and host outputs rotate: set i % 3 is
+            # reused by step i + 3 once step i's combine (the last reader of its pack, slot ids and flags) and
+            # its output copy are done. The expert outputs a step reads were last touched two steps (about
+            # twice a step's traffic, several times L2) earlier, so no L2 flush sits between the steps.
+            ce_out = mode == "pipelined-copy"
             ring = [step] + [P.MoeStep(w, dev, args.num_sms) for _ in range(2)]
             for r_ in ring[1:]:
                 r_.reset()
@@ -353,18 +356,19 @@ def run_native(args, rank, local_rank, world):
             copy_stream = torch.cuda.Stream(dev)
             disp_stream = torch.cuda.Stream(dev, priority=-1)  # a lower number is a higher priority
             comb_stream = torch.cuda.Stream(dev, priority=0)
-            side = (copy_stream, disp_stream, comb_stream)
+            out_stream = torch.cuda.Stream(dev)
+            side = (copy_stream, disp_stream, comb_stream, out_stream)
 
             def pipelined(n):
                 for s_ in side:
                     s_.wait_stream(stream)
                 copied = [torch.cuda.Event() for _ in range(n)]
                 dispatched = [torch.cuda.Event() for _ in range(n)]
-                done = [torch.cuda.Event() for _ in range(n)]
+                done = [torch.cuda.Event() for _ in range(n)]  # combine, and the output copy if any, finished
                 for i in range(n):
                     j = i % 3
                     if i >= 3:
-                        copy_stream.wait_event(done[i - 3])  # step i - 3 no longer reads set j
+                        copy_stream.wait_event(done[i - 3])  # step i - 3 no longer uses set j
                     with torch.cuda.stream(copy_stream):
                         dpacks[j].copy_(hpack, non_blocking=True)
                         copied[i].record(copy_stream)
@@ -378,8 +382,18 @@ def run_native(args, rank, local_rank, world):
                         dispatched[i].record(disp_stream)
                     comb_stream.wait_event(dispatched[i])
                     with torch.cuda.stream(comb_stream):
-                        ring[j].combine(d2s[j], out=hout_steps[j])
-                        done[i].record(comb_stream)
+                        if ce_out:
+                            ring[j].combine(d2s[j])
+                            combined = torch.cuda.Event()
+                            combined.record(comb_stream)
+                        else:
+                            ring[j].combine(d2s[j], out=hout_steps[j])
+                            done[i].record(comb_stream)
+                    if ce_out:
+                        out_stream.wait_event(combined)
+                        with torch.cuda.stream(out_stream):
+                            houts[j].copy_(ring[j].buf.out.view(w.num_tokens, w.hidden), non_blocking=True)
+                            done[i].record(out_stream)
                 for s_ in side:
                     stream.wait_stream(s_)
 
@@ -395,9 +409,12 @@ def run_native(args, rank, local_rank, world):
                 if r_.error() != B.MOE_OK:
                     raise RuntimeError("pipelined end-to-end steps latched an error")
             how = ("pipelined: each step's packed inputs copied in by a copy engine on its own stream; the step "
-                   "dispatches on a high-priority stream beside the previous step's combine, which writes the bf16 "
-                   "output straight into pinned host memory; three sets of step buffers, input packs and host "
-                   "outputs rotate instead of an L2 flush between steps")
+                   "dispatches on a high-priority stream beside the previous step's combine, "
+                   + ("which writes the bf16 output to device memory, and a second copy engine moves it to pinned "
+                      "host memory on a fourth stream; " if ce_out else
+                      "which writes the bf16 output straight into pinned host memory; ")
+                   + "three sets of step buffers, input packs and host outputs rotate instead of an L2 flush "
+                   "between steps")
         elif mode == "copy":
             d2 = inputs_in(dpack)
             for i in range(K):
@@ -438,7 +455,7 @@ def run_native(args, rank, local_rank, world):
             path(d)  # the same step on device buffers, to compare
             torch.cuda.synchronize()
         want = out_view.cpu().view(torch.int16)
-        for h_ in (houts if mode == "pipelined" else [hout]):
+        for h_ in (houts if mode.startswith("pipelined") else [hout]):
             if not torch.equal(h_.view(torch.int16), want):
                 raise RuntimeError("end-to-end output differs from the device output")
 
@@ -974,12 +991,13 @@ def main(argv=None):
     ap.add_argument("--calibrate", action="store_true",
                     help="print the bandwidth of plain device writes and copies at the step's sizes and exit")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-mode", choices=("auto", "hybrid", "zero-copy", "copy", "pipelined"), default="auto",
+    ap.add_argument("--e2e-mode", choices=("auto", "hybrid", "zero-copy", "copy", "pipelined", "pipelined-copy"), default="auto",
                     help="end to end: auto = pipelined up to 2048 tokens, zero-copy above; "
                          "hybrid = a copy engine moves the inputs in and combine writes the output "
                          "straight to pinned host memory; zero-copy = the kernels also read the inputs from host "
-                         "memory; copy = copy engines move both; pipelined = hybrid with each step's input copy "
-                         "overlapping the previous step")
+                         "memory; copy = copy engines move both; pipelined = hybrid with each step's input copy and "
+                         "dispatch overlapping the previous step's combine; pipelined-copy = pipelined with "
+                         "combine writing to device memory and a copy engine moving the output out")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)
