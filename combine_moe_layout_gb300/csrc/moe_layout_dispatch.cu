@@ -1,31 +1,41 @@
-// Layout and dispatch in one kernel, for batches whose per-rank routing fits
-// one CTA's shared memory (decode-sized batches).
+// Layout and dispatch in one kernel, for decode-sized batches (T <= 1024 tokens
+// per rank, rows of at most 16 KiB).
 //
 // Same results as moe_layout followed by moe_dispatch (Perplexity,
 // "Efficient and portable mixture-of-experts communication", section
 // "Dispatch": one warp counts the tokens per destination expert while the
 // other warps pack the tokens; "NVSHMEM and DeepEP: GPU-initiated
-// communication", low-latency section: fixed slots, no exchange). Here every
-// CTA is such a sender for a few rows of one source rank:
-//   - thread 0 starts the bulk TMA loads of its rows (x is an input, so this
-//     happens before waiting on the previous kernel);
-//   - all threads build the per-expert token bitmaps of the whole source rank
-//     (T bits per expert, T <= 1024) from topk_idx, which gives every count and
-//     every token-order slot position locally, with no grid-wide step and no
-//     wait on another CTA;
-//   - the CTA writes its rows' tok_slot entries, headers and scales, and thread
-//     0 writes each staged row into its k slots with bulk TMA stores;
-//   - the first CTA of each source rank writes counts and count + 1 flags.
-// A sender computes its own counts, so it needs no flag wait; the flags are
-// still written for the consumers of the step.
+// communication", low-latency section: fixed slots, no exchange). Every CTA is
+// such a sender for one row (src, t) at a time:
+//   1. all threads load the row into registers (32-byte vectors where the
+//      rows allow, else 16-byte ones), its scales and the row's k experts;
+//   2. the CTA reads the whole routing of rank src (L2-resident after the
+//      first CTA) and, per thread, counts the entries of earlier tokens equal
+//      to each of the row's k experts; warp reductions and one exchange in
+//      shared memory give pos_j = entries of tokens t' < t that chose e_j,
+//      i.e. the token-order position, with no grid-wide step and no wait on
+//      another CTA;
+//   3. the same pass histograms experts [t*G, (t+1)*G) (G = ceil(E / T)) over
+//      all of rank src's entries, so every (expert, source) count and its
+//      count + 1 flag is written by exactly one CTA;
+//   4. threads j < k write tok_slot and the slot headers, and every thread
+//      stores its vectors into the k slots (bf16 rows quantised to e4m3 on the
+//      way, for MOE_BF16_TO_FP8).
+// Nothing is read before griddepcontrol.wait, so every input may come from
+// the kernel immediately before this one in the stream.
+#include <climits>
+
 #include "moe_common.cuh"
 
 namespace moe {
 
 constexpr int kFusedThreads = 128;
+constexpr int kFusedWarps = kFusedThreads / 32;
 constexpr int kFusedMaxTokens = 1024;
-constexpr uint32_t kFusedMaxRowBytes = 16384;
-constexpr size_t kFusedMaxSmem = 96 * 1024;
+constexpr int kFusedMaxVec16 = 8;  // 16-byte vectors per thread: rows of at most 128 * 8 * 16 B = 16 KiB
+constexpr int kFusedMaxVec32 = 4;  // 32-byte vectors per thread: the same 16 KiB
+constexpr int kFusedMaxHist = 2048;       // experts one CTA histograms (G = ceil(E / T))
+constexpr int kFusedScanRegs = 2;        // int4 routing loads per thread issued with the row's loads
 
 struct FusedArgs {
   const int32_t *topk_idx;
@@ -38,197 +48,331 @@ struct FusedArgs {
   float *recv_scales;
   int4 *recv_meta;
   int32_t *err;
-  int R, T, E, k, max_m, nsc, words, ctas_per_rank, stages, early, quant;
-  uint32_t row_bytes;     // a dispatched row (the slot stride)
-  uint32_t in_row_bytes;  // a caller's input row (the stage size)
-  uint32_t qoff;          // quant mode: offset of the e4m3 row buffer in shared memory
-  int64_t nslots;
+  int R, T, E, k, max_m, nsc, G, early;
+  int vin;      // W-byte vectors of a caller's input row
+  int idx_vec;  // a rank's routing can be read as int4 (T*k % 4 == 0, 16-byte aligned base)
+  int sc_vec;   // scales move as float4 (nsc % 4 == 0, both scale arrays 16-byte aligned)
+  uint32_t row_bytes;     // a dispatched row: the slot stride of recv_x
+  uint32_t in_row_bytes;  // a caller's input row
+  int64_t nrows;
 };
 
-__global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArgs a) {
-  extern __shared__ __align__(128) uint8_t fsm[];
-  __shared__ uint64_t full[kMaxStages];
-  __shared__ int32_t dst[kMaxTopk];
-  __shared__ int aborted;
+// A W-byte piece of a row (W = 16 or 32), moved with one vector load and one
+// vector store per slot. 32-byte stores measured ~8 TB/s of writes on GB300
+// against ~5.5 TB/s for 16-byte ones, at the 60 MB a decode dispatch writes.
+template <int W>
+struct RowVec {
+  uint32_t w[W / 4];
+};
 
-  const int tid = threadIdx.x;
-  const int src = blockIdx.x / a.ctas_per_rank;
-  const int c = blockIdx.x % a.ctas_per_rank;
-  const int S = a.stages;
-  // rows t = c, c + C, c + 2C, ... of source rank src
-  const int n_mine = c < a.T ? (a.T - 1 - c) / a.ctas_per_rank + 1 : 0;
-  uint32_t *bits = reinterpret_cast<uint32_t *>(fsm + static_cast<size_t>(S) * a.in_row_bytes);
-  const uint8_t *xs = a.x + static_cast<int64_t>(src) * a.T * a.in_row_bytes;
-  uint8_t *qbuf = fsm + a.qoff;                                   // quant mode: e4m3 row
-  float *qsc = reinterpret_cast<float *>(fsm + a.qoff + a.row_bytes);  // quant mode: its scales
-
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
-    fence_mbar_init();
-    aborted = 0;
-    for (int i = 0; i < n_mine && i < S; ++i) {
-      const int t = c + i * a.ctas_per_rank;
-      mbar_arrive_expect_tx(&full[i], a.in_row_bytes);
-      bulk_load(fsm + static_cast<size_t>(i) * a.in_row_bytes, xs + static_cast<int64_t>(t) * a.in_row_bytes,
-                a.in_row_bytes, &full[i]);
-    }
+// Read-once load (evict-first) of a row piece; volatile keeps it ahead of the
+// CTA barriers that follow, so its latency overlaps the layout work.
+template <int W>
+__device__ __forceinline__ RowVec<W> ld_row(const uint8_t *p) {
+  RowVec<W> r;
+  if constexpr (W == 32) {
+    asm volatile("ld.global.cs.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]), "=r"(r.w[5]),
+                   "=r"(r.w[6]), "=r"(r.w[7])
+                 : "l"(p));
+  } else {
+    asm volatile("ld.global.cs.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3])
+                 : "l"(p));
   }
+  return r;
+}
+
+template <int W>
+__device__ __forceinline__ void st_row(uint8_t *p, const RowVec<W> &r) {
+  if constexpr (W == 32) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r.w[0]), "r"(r.w[1]),
+                 "r"(r.w[2]), "r"(r.w[3]), "r"(r.w[4]), "r"(r.w[5]), "r"(r.w[6]), "r"(r.w[7])
+                 : "memory");
+  } else {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(r.w[0]), "r"(r.w[1]), "r"(r.w[2]),
+                 "r"(r.w[3])
+                 : "memory");
+  }
+}
+
+template <int W, int VPT, int KC, bool QUANT>
+__global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArgs a) {
+  __shared__ int32_t s_part[kFusedWarps][KC];
+  __shared__ int32_t s_own[KC];
+  __shared__ int32_t s_slot[KC];
+  extern __shared__ int32_t s_hist[];  // [G]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // every input (x, x_scales, topk_idx) may be written by the previous kernel
   grid_dependency_wait();
   if (a.early) grid_dependents_launch();
 
-  // per-expert token bitmaps of the whole source rank
-  for (int i = tid; i < a.E * a.words; i += kFusedThreads) bits[i] = 0;
-  __syncthreads();
-  const int32_t *idx = a.topk_idx + static_cast<int64_t>(src) * a.T * a.k;
-  for (int i = tid; i < a.T * a.k; i += kFusedThreads) {
-    const int e = __ldg(idx + i);
-    if (e < 0 || e >= a.E) {
-      if (e != kMaskedExpert) latch_error(a.err, MOE_EINVAL);  // a masked choice is skipped silently
-      continue;
-    }
-    const int t = i / a.k;
-    const uint32_t bit = 1u << (t & 31);
-    if (atomicOr(&bits[e * a.words + (t >> 5)], bit) & bit) latch_error(a.err, MOE_EINVAL);
-  }
-  __syncthreads();
+  const int n = a.T * a.k;  // routing entries of a rank
+  for (int64_t row = blockIdx.x; row < a.nrows; row += gridDim.x) {
+    const int src = static_cast<int>(row / a.T);
+    const int t = static_cast<int>(row - static_cast<int64_t>(src) * a.T);
+    const int32_t *ridx = a.topk_idx + static_cast<int64_t>(src) * a.T * a.k;  // routing of rank src
+    const int32_t *own_p = ridx + static_cast<int64_t>(t) * a.k;
 
-  if (c == 0) {
-    for (int e = tid; e < a.E; e += kFusedThreads) {
-      int cnt = 0;
-      for (int w = 0; w < a.words; ++w) cnt += __popc(bits[e * a.words + w]);
-      const int64_t r = static_cast<int64_t>(e) * a.R + src;
-      a.counts[r] = cnt;
-      a.flags[r] = static_cast<uint64_t>(cnt) + 1;
+    // 1. every load of the row at once: the row, its scales, its experts and
+    //    the first kFusedScanRegs entries per thread of the rank's routing
+    RowVec<W> v[VPT];
+    const uint8_t *xr = a.x + row * a.in_row_bytes;
+#pragma unroll
+    for (int u = 0; u < VPT; ++u) {
+      const int q = tid + u * kFusedThreads;
+      if (q < a.vin) {
+        v[u] = ld_row<W>(xr + static_cast<int64_t>(q) * W);
+      } else {
+#pragma unroll
+        for (int z = 0; z < W / 4; ++z) v[u].w[z] = 0;
+      }
     }
-  }
-
-  int i = 0;
-  for (; i < n_mine; ++i) {
-    const int s = i % S;
-    const uint32_t parity = static_cast<uint32_t>((i / S) & 1);
-    const int t = c + i * a.ctas_per_rank;
-    const int64_t row = static_cast<int64_t>(src) * a.T + t;
+    float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!QUANT && a.nsc > 0) {
+      const float *xs = a.x_scales + row * a.nsc;
+      if (a.sc_vec) {
+        if (tid < a.nsc / 4) sc = __ldcs(reinterpret_cast<const float4 *>(xs) + tid);
+      } else if (tid < a.nsc) {
+        sc.x = __ldcs(xs + tid);
+      }
+    }
+    int4 r4[kFusedScanRegs];
+    if (a.idx_vec) {
+#pragma unroll
+      for (int c = 0; c < kFusedScanRegs; ++c) {
+        const int q = tid + c * kFusedThreads;
+        r4[c] = q < n / 4 ? __ldcg(reinterpret_cast<const int4 *>(ridx) + q) : make_int4(-1, -1, -1, -1);
+      }
+    }
     if (tid < a.k) {
-      const int e = __ldg(idx + t * a.k + tid);
+      const int e = __ldcg(own_p + tid);
+      s_own[tid] = (e >= 0 && e < a.E) ? e : INT_MIN;  // INT_MIN matches no entry
+    }
+    const int h0 = t * a.G;
+    const int hn = max(0, min(a.G, a.E - h0));
+    for (int i = tid; i < hn; i += kFusedThreads) s_hist[i] = 0;
+    __syncthreads();
+
+    // 2-3. earlier entries per own expert, and the histogram of experts [h0, h0 + hn)
+    int own[KC], cnt[KC];
+#pragma unroll
+    for (int j = 0; j < KC; ++j) {
+      own[j] = j < a.k ? s_own[j] : INT_MIN;
+      cnt[j] = 0;
+    }
+    const int before = t * a.k;
+    auto visit = [&](int i, int e) {
+      if (i < before) {
+#pragma unroll
+        for (int j = 0; j < KC; ++j) cnt[j] += e == own[j];
+      }
+      const unsigned hb = static_cast<unsigned>(e - h0);  // masked and invalid ids fall outside
+      if (hb < static_cast<unsigned>(hn)) atomicAdd(&s_hist[hb], 1);
+    };
+    if (a.idx_vec) {
+#pragma unroll
+      for (int c = 0; c < kFusedScanRegs; ++c) {
+        const int q = tid + c * kFusedThreads;
+        visit(4 * q, r4[c].x);
+        visit(4 * q + 1, r4[c].y);
+        visit(4 * q + 2, r4[c].z);
+        visit(4 * q + 3, r4[c].w);
+      }
+      for (int q = tid + kFusedScanRegs * kFusedThreads; q < n / 4; q += kFusedThreads) {
+        const int4 e4 = __ldcg(reinterpret_cast<const int4 *>(ridx) + q);
+        visit(4 * q, e4.x);
+        visit(4 * q + 1, e4.y);
+        visit(4 * q + 2, e4.z);
+        visit(4 * q + 3, e4.w);
+      }
+    } else {
+      for (int i = tid; i < n; i += kFusedThreads) visit(i, __ldcg(ridx + i));
+    }
+#pragma unroll
+    for (int j = 0; j < KC; ++j) {
+      const int c = __reduce_add_sync(0xffffffffu, cnt[j]);
+      if (lane == 0) s_part[warp][j] = c;
+    }
+    __syncthreads();
+
+    // 4. slots, headers, counts and flags
+    if (tid < a.k) {
+      const int e = s_own[tid];
       int32_t slot = -1;
-      if (e >= 0 && e < a.E) {
-        const uint32_t *b = bits + e * a.words;
+      if (e != INT_MIN) {
         int pos = 0;
-        for (int w = 0; w < (t >> 5); ++w) pos += __popc(b[w]);
-        pos += __popc(b[t >> 5] & ((1u << (t & 31)) - 1u));
+#pragma unroll
+        for (int w = 0; w < kFusedWarps; ++w) pos += s_part[w][tid];
         if (pos < a.max_m)
           slot = static_cast<int32_t>((static_cast<int64_t>(e) * a.R + src) * a.max_m + pos);
         else
           latch_error(a.err, MOE_EOVERFLOW);
+        for (int j = 0; j < tid; ++j)
+          if (s_own[j] == e) latch_error(a.err, MOE_EINVAL);  // expert repeated within the token
+        if (slot >= 0) a.recv_meta[slot] = make_int4(src, t, e, tid);
+      } else if (__ldcg(own_p + tid) != kMaskedExpert) {
+        latch_error(a.err, MOE_EINVAL);  // a masked choice is skipped silently
       }
       a.tok_slot[row * a.k + tid] = slot;
-      dst[tid] = slot;
-      if (slot >= 0) a.recv_meta[slot] = make_int4(src, t, e, tid);
+      s_slot[tid] = slot;
+    }
+    for (int i = tid; i < hn; i += kFusedThreads) {
+      const int c = s_hist[i];
+      const int64_t r = static_cast<int64_t>(h0 + i) * a.R + src;
+      a.counts[r] = c;
+      a.flags[r] = static_cast<uint64_t>(c) + 1;
     }
     __syncthreads();
-    if (a.quant) {
-      uint8_t *stage = fsm + static_cast<size_t>(s) * a.in_row_bytes;
-      if (!mbar_wait_bounded(&full[s], parity)) {  // every thread reads the staged bf16 row
-        latch_error(a.err, MOE_ETIMEOUT);
-        aborted = 1;
-      }
-      if (tid == 0 && i > 0) bulk_wait_read<0>();  // the previous row's stores may still read qbuf
-      __syncthreads();
-      if (aborted) break;
-      quantize_blocks(reinterpret_cast<const uint16_t *>(stage), qbuf, qsc, a.nsc, tid >> 5, kFusedThreads / 32,
-                      tid & 31);
-      fence_proxy_async_smem();  // the shared writes above, before the bulk stores and the refill
-      __syncthreads();
-      for (int q = tid; q < a.k * a.nsc; q += kFusedThreads) {
-        const int j = q / a.nsc, cc = q - j * a.nsc;
-        const int32_t slot = dst[j];
-        if (slot >= 0) a.recv_scales[static_cast<int64_t>(slot) * a.nsc + cc] = qsc[cc];
-      }
-      if (tid == 0) {
-        for (int j = 0; j < a.k; ++j)
-          if (dst[j] >= 0) bulk_store(a.recv_x + static_cast<int64_t>(dst[j]) * a.row_bytes, qbuf, a.row_bytes);
-        bulk_commit();
-        if (i + S < n_mine) {  // the bf16 stage has been consumed: refill it with row i + S
-          const int tn = c + (i + S) * a.ctas_per_rank;
-          mbar_arrive_expect_tx(&full[s], a.in_row_bytes);
-          bulk_load(stage, xs + static_cast<int64_t>(tn) * a.in_row_bytes, a.in_row_bytes, &full[s]);
+
+    // 5. the k copies
+    if constexpr (!QUANT) {
+#pragma unroll
+      for (int j = 0; j < KC; ++j) {
+        if (j >= a.k) break;
+        const int32_t slot = s_slot[j];
+        if (slot < 0) continue;
+        uint8_t *dst = a.recv_x + static_cast<int64_t>(slot) * a.row_bytes;
+#pragma unroll
+        for (int u = 0; u < VPT; ++u) {
+          const int q = tid + u * kFusedThreads;
+          if (q < a.vin) st_row<W>(dst + static_cast<int64_t>(q) * W, v[u]);
+        }
+        if (a.nsc > 0) {
+          float *ds = a.recv_scales + static_cast<int64_t>(slot) * a.nsc;
+          if (a.sc_vec) {
+            if (tid < a.nsc / 4) reinterpret_cast<float4 *>(ds)[tid] = sc;
+          } else if (tid < a.nsc) {
+            ds[tid] = sc.x;
+          }
         }
       }
-      __syncthreads();
-      continue;
-    }
-    if (a.nsc > 0) {
-      const float *sc = a.x_scales + row * a.nsc;
-      for (int q = tid; q < a.k * a.nsc; q += kFusedThreads) {
-        const int j = q / a.nsc, cc = q - j * a.nsc;
-        const int32_t slot = dst[j];
-        if (slot >= 0) a.recv_scales[static_cast<int64_t>(slot) * a.nsc + cc] = __ldg(sc + cc);
-      }
-    }
-    if (tid == 0) {
-      uint8_t *stage = fsm + static_cast<size_t>(s) * a.in_row_bytes;
-      if (!mbar_wait_bounded(&full[s], parity)) {
-        latch_error(a.err, MOE_ETIMEOUT);
-        aborted = 1;
-      } else {
-        for (int j = 0; j < a.k; ++j)
-          if (dst[j] >= 0) bulk_store(a.recv_x + static_cast<int64_t>(dst[j]) * a.row_bytes, stage, a.row_bytes);
-        bulk_commit();
-        const int next = i - 1 + S;
-        if (i >= 1 && next < n_mine) {
-          bulk_wait_read<1>();
-          const int ps = (i - 1) % S;
-          const int tn = c + next * a.ctas_per_rank;
-          mbar_arrive_expect_tx(&full[ps], a.in_row_bytes);
-          bulk_load(fsm + static_cast<size_t>(ps) * a.in_row_bytes, xs + static_cast<int64_t>(tn) * a.in_row_bytes,
-                    a.in_row_bytes, &full[ps]);
+    } else {
+      // Quantise on dispatch. Vector q holds bf16 elements (W/2)q .. (W/2)q +
+      // W/2 - 1, so a 128-element block is G = 256 / W consecutive lanes (vin is
+      // a multiple of G). scale = amax / 448 (1 for an all-zero block), code =
+      // e4m3(x / scale) with IEEE fp32 division and the hardware's nearest-even
+      // saturating conversion; W/2 codes per thread.
+      constexpr int NE = W / 2;         // bf16 elements per vector
+      constexpr int G = 256 / W;        // lanes per 128-element block
+#pragma unroll
+      for (int u = 0; u < VPT; ++u) {
+        const int q = tid + u * kFusedThreads;
+        float f[NE];
+#pragma unroll
+        for (int p = 0; p < NE / 2; ++p) {
+          f[2 * p] = __uint_as_float(v[u].w[p] << 16);
+          f[2 * p + 1] = __uint_as_float(v[u].w[p] & 0xffff0000u);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int p = 0; p < NE; ++p) amax = fmaxf(amax, fabsf(f[p]));
+#pragma unroll
+        for (int o = G / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+        uint32_t c[NE / 4];
+#pragma unroll
+        for (int p = 0; p < NE / 4; ++p)
+          c[p] = static_cast<uint32_t>(e4m3x2_rn_satfinite(__fdiv_rn(f[4 * p], s), __fdiv_rn(f[4 * p + 1], s))) |
+                 (static_cast<uint32_t>(e4m3x2_rn_satfinite(__fdiv_rn(f[4 * p + 2], s), __fdiv_rn(f[4 * p + 3], s)))
+                  << 16);
+        // 16-byte stores: 32-byte vectors give 16 codes each; 16-byte vectors
+        // give 8, so even lanes take their odd neighbour's 8 as well
+        uint4 out16;
+        bool store16;
+        if constexpr (W == 32) {
+          out16 = make_uint4(c[0], c[1], c[2], c[3]);
+          store16 = true;
+        } else {
+          const uint32_t px = __shfl_xor_sync(0xffffffffu, c[0], 1);
+          const uint32_t py = __shfl_xor_sync(0xffffffffu, c[1], 1);
+          out16 = make_uint4(c[0], c[1], px, py);
+          store16 = (q & 1) == 0;
+        }
+        if (q >= a.vin) continue;  // whole G-lane groups are out together
+#pragma unroll
+        for (int j = 0; j < KC; ++j) {
+          if (j >= a.k) break;
+          const int32_t slot = s_slot[j];
+          if (slot < 0) continue;
+          uint8_t *dst = a.recv_x + static_cast<int64_t>(slot) * a.row_bytes;
+          if (store16) *reinterpret_cast<uint4 *>(dst + static_cast<int64_t>(q) * NE) = out16;
+          if (q % G == 0) a.recv_scales[static_cast<int64_t>(slot) * a.nsc + q / G] = s;
         }
       }
     }
-    __syncthreads();
-    if (aborted) break;
-  }
-  if (tid == 0) {
-    if (aborted) {
-      // drain the loads still in flight (bounded) before the CTA releases its shared memory
-      const int issued = a.quant ? min(n_mine, i + S) : static_cast<int>(inflight_end(i, S, n_mine));
-      for (int u = i; u < issued; ++u) mbar_wait_bounded(&full[u % S], static_cast<uint32_t>((u / S) & 1));
-    }
-    bulk_wait_all();
   }
 }
 
-// Offset of the e4m3 row buffer (quant mode): after the row stages and the bitmaps.
-static size_t fused_qoff(const Sizes &s, int stages) {
-  const int words = (s.T + 31) / 32;
-  const size_t end = static_cast<size_t>(stages) * s.in_row_bytes + static_cast<size_t>(s.E) * (words > 0 ? words : 1) * 4;
-  return (end + 127) / 128 * 128;
+// Vectors per thread of the fused kernel (a power of two covering vin, at most
+// max_vpt), or 0 when a row is too long.
+static int fused_vpt(int64_t vin, int max_vpt) {
+  const int64_t need = (vin + kFusedThreads - 1) / kFusedThreads;
+  for (int p = 1; p <= max_vpt; p *= 2)
+    if (need <= p) return p;
+  return 0;
 }
 
-// Whether one CTA can hold a source rank's bitmaps next to its row stages.
-static bool fused_fits(const Sizes &s, int stages, size_t *smem) {
-  if (s.T > kFusedMaxTokens || s.in_row_bytes > kFusedMaxRowBytes || s.in_row_bytes % 16 != 0) return false;
-  const int words = (s.T + 31) / 32;
-  *smem = static_cast<size_t>(stages) * s.in_row_bytes + static_cast<size_t>(s.E) * (words > 0 ? words : 1) * 4;
-  if (s.quant) *smem = fused_qoff(s, stages) + static_cast<size_t>(s.row_bytes) + static_cast<size_t>(s.nsc) * 4;
-  return *smem <= kFusedMaxSmem;
+static int fused_hist(const Sizes &s) { return s.T > 0 ? (s.E + s.T - 1) / s.T : s.E; }
+
+// Whether the batch runs as the one fused kernel (rows of at most 16 KiB).
+static bool fused_fits(const Sizes &s) {
+  if (s.ntok == 0 || s.T > kFusedMaxTokens || s.in_row_bytes % 16 != 0) return false;
+  if (fused_vpt(s.in_row_bytes / 16, kFusedMaxVec16) == 0) return false;
+  return fused_hist(s) <= kFusedMaxHist;
 }
 
-int layout_dispatch_kernel_count(const Sizes &s) {
-  size_t smem = 0;
-  return (s.ntok == 0 || !fused_fits(s, 2, &smem)) ? (s.ntok == 0 ? 1 : 2) : 1;
+int layout_dispatch_kernel_count(const Sizes &s) { return (s.ntok == 0 || fused_fits(s)) ? 1 : 2; }
+
+template <int W, int VPT, int KC, bool QUANT>
+static moe_status launch_fused(const FusedArgs &a, int sms, cudaStream_t stream) {
+  auto kern = layout_dispatch_kernel<W, VPT, KC, QUANT>;
+  const size_t smem = static_cast<size_t>(a.G) * sizeof(int32_t);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return MOE_ECUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFusedThreads, smem) != cudaSuccess)
+    return MOE_ECUDA;
+  if (per_sm < 1) return MOE_EINVAL;
+  // one row per CTA while every CTA is resident at once; beyond that, CTAs loop
+  const int64_t capacity = static_cast<int64_t>(sms) * per_sm;
+  const int64_t grid = a.nrows < capacity ? a.nrows : capacity;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kFusedThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  use_pdl(cfg, attr);
+  if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return MOE_ECUDA;
+  return launch_status();
+}
+
+template <int KC, bool QUANT>
+static moe_status launch_fused_w(const FusedArgs &a, bool wide, int sms, cudaStream_t stream) {
+  if (!wide) return launch_fused<16, kFusedMaxVec16, kMaxTopk, QUANT>(a, sms, stream);
+  switch (fused_vpt(a.vin, kFusedMaxVec32)) {
+    case 1: return launch_fused<32, 1, KC, QUANT>(a, sms, stream);
+    case 2: return launch_fused<32, 2, KC, QUANT>(a, sms, stream);
+    case 4: return launch_fused<32, 4, KC, QUANT>(a, sms, stream);
+    default: return MOE_EINVAL;
+  }
 }
 
 moe_status launch_layout_dispatch(const Sizes &s, const int32_t *topk_idx, const void *x, const float *x_scales,
                                   int32_t *counts, uint64_t *flags, int32_t *tok_slot, void *recv_x,
                                   float *recv_scales, int32_t *recv_meta, int32_t *err, int num_sms,
                                   cudaStream_t stream) {
-  size_t smem = 0;
-  if (s.ntok == 0 || !fused_fits(s, 2, &smem)) {
+  if (!fused_fits(s)) {
     moe_status st = launch_layout(s, topk_idx, counts, flags, tok_slot, err, stream);
-    if (st != MOE_OK) return st;
+    if (st != MOE_OK || s.ntok == 0) return st;
     return launch_dispatch(s, x, x_scales, tok_slot, flags, recv_x, recv_scales, recv_meta, err, num_sms, stream);
   }
+  // 32-byte vectors when the input rows and (copy mode) the slot rows allow them
+  const bool wide = s.in_row_bytes % 32 == 0 && aligned32(x) &&
+                    (s.quant || (s.row_bytes % 32 == 0 && aligned32(recv_x)));
   FusedArgs a{};
   a.topk_idx = topk_idx;
   a.counts = counts;
@@ -246,45 +390,19 @@ moe_status launch_layout_dispatch(const Sizes &s, const int32_t *topk_idx, const
   a.k = s.k;
   a.max_m = s.max_m;
   a.nsc = s.nsc;
-  a.words = (s.T + 31) / 32;
+  a.G = fused_hist(s);
   a.early = early_trigger(s.ntok);
-  a.quant = s.quant ? 1 : 0;
+  a.vin = static_cast<int>(s.in_row_bytes / (wide ? 32 : 16));
+  a.idx_vec = (static_cast<int64_t>(s.T) * s.k) % 4 == 0 && aligned16(topk_idx) ? 1 : 0;
+  a.sc_vec = s.nsc % 4 == 0 && aligned16(x_scales) && aligned16(recv_scales) ? 1 : 0;
   a.row_bytes = static_cast<uint32_t>(s.row_bytes);
   a.in_row_bytes = static_cast<uint32_t>(s.in_row_bytes);
-  a.nslots = s.nslots;
-
+  a.nrows = s.ntok;
   const int sms = num_sms > 0 && num_sms < sm_count() ? num_sms : sm_count();
-  // first try one row per CTA (one stage); with fewer CTAs than rows use two stages
-  for (int stages = 1; stages <= 2; ++stages) {
-    if (!fused_fits(s, stages, &smem)) return MOE_EINVAL;
-    a.qoff = static_cast<uint32_t>(fused_qoff(s, stages));
-    if (smem > 48 * 1024 && cudaFuncSetAttribute(layout_dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem)) != cudaSuccess)
-      return MOE_ECUDA;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layout_dispatch_kernel, kFusedThreads, smem) !=
-        cudaSuccess)
-      return MOE_ECUDA;
-    if (per_sm < 1) return MOE_EINVAL;
-    const int64_t capacity = static_cast<int64_t>(sms) * per_sm;
-    int64_t per_rank = capacity / s.R;
-    if (per_rank < 1) per_rank = 1;
-    if (per_rank > s.T) per_rank = s.T;
-    const int rows = static_cast<int>((s.T + per_rank - 1) / per_rank);
-    if (rows > 1 && stages == 1) continue;
-    a.ctas_per_rank = static_cast<int>(per_rank);
-    a.stages = stages;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(per_rank * s.R), 1, 1);
-    cfg.blockDim = dim3(kFusedThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    use_pdl(cfg, attr);
-    if (cudaLaunchKernelEx(&cfg, layout_dispatch_kernel, a) != cudaSuccess) return MOE_ECUDA;
-    return launch_status();
-  }
-  return MOE_EINVAL;
+  if (s.k <= 8)
+    return s.quant ? launch_fused_w<8, true>(a, wide, sms, stream) : launch_fused_w<8, false>(a, wide, sms, stream);
+  return s.quant ? launch_fused_w<kMaxTopk, true>(a, wide, sms, stream)
+                 : launch_fused_w<kMaxTopk, false>(a, wide, sms, stream);
 }
 
 }  // namespace moe
