@@ -9,18 +9,19 @@
 // such a sender for one row (src, t) at a time:
 //   1. all threads load the row into registers (32-byte vectors where the
 //      rows allow, else 16-byte ones), its scales and the row's k experts;
-//   2. the CTA reads the whole routing of rank src (L2-resident after the
-//      first CTA) and, per thread, counts the entries of earlier tokens equal
-//      to each of the row's k experts; warp reductions and one exchange in
-//      shared memory give pos_j = entries of tokens t' < t that chose e_j,
+//   2. the CTA reads the routing entries of rank src's earlier tokens
+//      (L2-resident after the first CTA) and, per thread, counts the entries
+//      equal to each of the row's k experts; warp reductions and one exchange
+//      in shared memory give pos_j = entries of tokens t' < t that chose e_j,
 //      i.e. the token-order position, with no grid-wide step and no wait on
 //      another CTA;
-//   3. the same pass histograms experts [t*G, (t+1)*G) (G = ceil(E / T)) over
-//      all of rank src's entries, so every (expert, source) count and its
+//   3. the last 32 rows of a rank read all of its entries and also histogram
+//      a share of the experts, so every (expert, source) count and its
 //      count + 1 flag is written by exactly one CTA;
-//   4. threads j < k write tok_slot and the slot headers, and every thread
-//      stores its vectors into the k slots (bf16 rows quantised to e4m3 on the
-//      way, for MOE_BF16_TO_FP8).
+//   4. every thread stores its vectors into the k slots (bf16 rows quantised
+//      to e4m3 on the way, for MOE_BF16_TO_FP8); only then are tok_slot, the
+//      slot headers, counts and flags written, so a CTA's copies never queue
+//      behind them.
 // Nothing is read before griddepcontrol.wait, so every input may come from
 // the kernel immediately before this one in the stream.
 #include <climits>
@@ -36,6 +37,7 @@ constexpr int kFusedMaxVec16 = 8;  // 16-byte vectors per thread: rows of at mos
 constexpr int kFusedMaxVec32 = 4;  // 32-byte vectors per thread: the same 16 KiB
 constexpr int kFusedMaxHist = 2048;       // experts one CTA histograms (G = ceil(E / T))
 constexpr int kFusedScanRegs = 2;        // int4 routing loads per thread issued with the row's loads
+constexpr int kFusedHistRows = 32;       // rows per rank that also count experts for counts and flags
 
 struct FusedArgs {
   const int32_t *topk_idx;
@@ -83,15 +85,26 @@ __device__ __forceinline__ RowVec<W> ld_row(const uint8_t *p) {
   return r;
 }
 
+// L2 policy of the slot rows: evict last. The experts read the slots next, and
+// the combine that follows a step reads 117 MB (decode) through L2: measured on
+// GB300, with the 60 MB of slot rows held at normal priority that combine took
+// 26.4 us, with evict-last 24.7 us, the same as after a clean L2.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 template <int W>
-__device__ __forceinline__ void st_row(uint8_t *p, const RowVec<W> &r) {
+__device__ __forceinline__ void st_row(uint8_t *p, const RowVec<W> &r, uint64_t pol) {
   if constexpr (W == 32) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r.w[0]), "r"(r.w[1]),
-                 "r"(r.w[2]), "r"(r.w[3]), "r"(r.w[4]), "r"(r.w[5]), "r"(r.w[6]), "r"(r.w[7])
+    asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p),
+                 "r"(r.w[0]), "r"(r.w[1]), "r"(r.w[2]), "r"(r.w[3]), "r"(r.w[4]), "r"(r.w[5]), "r"(r.w[6]),
+                 "r"(r.w[7]), "l"(pol)
                  : "memory");
   } else {
-    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(r.w[0]), "r"(r.w[1]), "r"(r.w[2]),
-                 "r"(r.w[3])
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(r.w[0]), "r"(r.w[1]),
+                 "r"(r.w[2]), "r"(r.w[3]), "l"(pol)
                  : "memory");
   }
 }
@@ -109,6 +122,7 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
   if (a.early) grid_dependents_launch();
 
   const int n = a.T * a.k;  // routing entries of a rank
+  const int hist_rows = min(a.T, kFusedHistRows);
   for (int64_t row = blockIdx.x; row < a.nrows; row += gridDim.x) {
     const int src = static_cast<int>(row / a.T);
     const int t = static_cast<int>(row - static_cast<int64_t>(src) * a.T);
@@ -138,20 +152,26 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
         sc.x = __ldcs(xs + tid);
       }
     }
+    // The last hist_rows rows of a rank also count experts [h0, h0 + hn) over
+    // all of its entries (they visit nearly all of them anyway); the other rows
+    // visit only the entries of earlier tokens.
+    const int hr = t - (a.T - hist_rows);
+    const int h0 = hr >= 0 ? hr * a.G : 0;
+    const int hn = hr >= 0 ? max(0, min(a.G, a.E - h0)) : 0;
+    const int before = t * a.k;
+    const int m = hn > 0 ? n : before;  // entries this CTA visits
     int4 r4[kFusedScanRegs];
     if (a.idx_vec) {
 #pragma unroll
       for (int c = 0; c < kFusedScanRegs; ++c) {
         const int q = tid + c * kFusedThreads;
-        r4[c] = q < n / 4 ? __ldcg(reinterpret_cast<const int4 *>(ridx) + q) : make_int4(-1, -1, -1, -1);
+        r4[c] = 4 * q < m ? __ldcg(reinterpret_cast<const int4 *>(ridx) + q) : make_int4(-1, -1, -1, -1);
       }
     }
     if (tid < a.k) {
       const int e = __ldcg(own_p + tid);
       s_own[tid] = (e >= 0 && e < a.E) ? e : INT_MIN;  // INT_MIN matches no entry
     }
-    const int h0 = t * a.G;
-    const int hn = max(0, min(a.G, a.E - h0));
     for (int i = tid; i < hn; i += kFusedThreads) s_hist[i] = 0;
     __syncthreads();
 
@@ -162,7 +182,6 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
       own[j] = j < a.k ? s_own[j] : INT_MIN;
       cnt[j] = 0;
     }
-    const int before = t * a.k;
     auto visit = [&](int i, int e) {
       if (i < before) {
 #pragma unroll
@@ -175,12 +194,14 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
 #pragma unroll
       for (int c = 0; c < kFusedScanRegs; ++c) {
         const int q = tid + c * kFusedThreads;
-        visit(4 * q, r4[c].x);
-        visit(4 * q + 1, r4[c].y);
-        visit(4 * q + 2, r4[c].z);
-        visit(4 * q + 3, r4[c].w);
+        if (4 * q < m) {
+          visit(4 * q, r4[c].x);
+          visit(4 * q + 1, r4[c].y);
+          visit(4 * q + 2, r4[c].z);
+          visit(4 * q + 3, r4[c].w);
+        }
       }
-      for (int q = tid + kFusedScanRegs * kFusedThreads; q < n / 4; q += kFusedThreads) {
+      for (int q = tid + kFusedScanRegs * kFusedThreads; 4 * q < m; q += kFusedThreads) {
         const int4 e4 = __ldcg(reinterpret_cast<const int4 *>(ridx) + q);
         visit(4 * q, e4.x);
         visit(4 * q + 1, e4.y);
@@ -188,7 +209,7 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
         visit(4 * q + 3, e4.w);
       }
     } else {
-      for (int i = tid; i < n; i += kFusedThreads) visit(i, __ldcg(ridx + i));
+      for (int i = tid; i < m; i += kFusedThreads) visit(i, __ldcg(ridx + i));
     }
 #pragma unroll
     for (int j = 0; j < KC; ++j) {
@@ -197,36 +218,31 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
     }
     __syncthreads();
 
-    // 4. slots, headers, counts and flags
+    // 4. the row's slots
+    int32_t my_slot = -1;
+    int my_e = 0;
     if (tid < a.k) {
       const int e = s_own[tid];
-      int32_t slot = -1;
       if (e != INT_MIN) {
         int pos = 0;
 #pragma unroll
         for (int w = 0; w < kFusedWarps; ++w) pos += s_part[w][tid];
         if (pos < a.max_m)
-          slot = static_cast<int32_t>((static_cast<int64_t>(e) * a.R + src) * a.max_m + pos);
+          my_slot = static_cast<int32_t>((static_cast<int64_t>(e) * a.R + src) * a.max_m + pos);
         else
           latch_error(a.err, MOE_EOVERFLOW);
         for (int j = 0; j < tid; ++j)
           if (s_own[j] == e) latch_error(a.err, MOE_EINVAL);  // expert repeated within the token
-        if (slot >= 0) a.recv_meta[slot] = make_int4(src, t, e, tid);
       } else if (__ldcg(own_p + tid) != kMaskedExpert) {
         latch_error(a.err, MOE_EINVAL);  // a masked choice is skipped silently
       }
-      a.tok_slot[row * a.k + tid] = slot;
-      s_slot[tid] = slot;
-    }
-    for (int i = tid; i < hn; i += kFusedThreads) {
-      const int c = s_hist[i];
-      const int64_t r = static_cast<int64_t>(h0 + i) * a.R + src;
-      a.counts[r] = c;
-      a.flags[r] = static_cast<uint64_t>(c) + 1;
+      my_e = e;
+      s_slot[tid] = my_slot;
     }
     __syncthreads();
 
     // 5. the k copies
+    const uint64_t pol = l2_evict_last_policy();
     if constexpr (!QUANT) {
 #pragma unroll
       for (int j = 0; j < KC; ++j) {
@@ -237,7 +253,7 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
 #pragma unroll
         for (int u = 0; u < VPT; ++u) {
           const int q = tid + u * kFusedThreads;
-          if (q < a.vin) st_row<W>(dst + static_cast<int64_t>(q) * W, v[u]);
+          if (q < a.vin) st_row<W>(dst + static_cast<int64_t>(q) * W, v[u], pol);
         }
         if (a.nsc > 0) {
           float *ds = a.recv_scales + static_cast<int64_t>(slot) * a.nsc;
@@ -279,15 +295,15 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
                   << 16);
         // 16-byte stores: 32-byte vectors give 16 codes each; 16-byte vectors
         // give 8, so even lanes take their odd neighbour's 8 as well
-        uint4 out16;
+        RowVec<16> out16;
         bool store16;
         if constexpr (W == 32) {
-          out16 = make_uint4(c[0], c[1], c[2], c[3]);
+          out16 = RowVec<16>{{c[0], c[1], c[2], c[3]}};
           store16 = true;
         } else {
           const uint32_t px = __shfl_xor_sync(0xffffffffu, c[0], 1);
           const uint32_t py = __shfl_xor_sync(0xffffffffu, c[1], 1);
-          out16 = make_uint4(c[0], c[1], px, py);
+          out16 = RowVec<16>{{c[0], c[1], px, py}};
           store16 = (q & 1) == 0;
         }
         if (q >= a.vin) continue;  // whole G-lane groups are out together
@@ -297,11 +313,26 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
           const int32_t slot = s_slot[j];
           if (slot < 0) continue;
           uint8_t *dst = a.recv_x + static_cast<int64_t>(slot) * a.row_bytes;
-          if (store16) *reinterpret_cast<uint4 *>(dst + static_cast<int64_t>(q) * NE) = out16;
+          if (store16) st_row<16>(dst + static_cast<int64_t>(q) * NE, out16, pol);
           if (q % G == 0) a.recv_scales[static_cast<int64_t>(slot) * a.nsc + q / G] = s;
         }
       }
     }
+
+    // 6. the step's records, after the copies (nothing above waits for them):
+    //    tok_slot, the slot headers, and the counts and count + 1 flags of
+    //    this row's share of the experts
+    if (tid < a.k) {
+      a.tok_slot[row * a.k + tid] = my_slot;
+      if (my_slot >= 0) a.recv_meta[my_slot] = make_int4(src, t, my_e, tid);
+    }
+    for (int i = tid; i < hn; i += kFusedThreads) {
+      const int c = s_hist[i];
+      const int64_t r = static_cast<int64_t>(h0 + i) * a.R + src;
+      a.counts[r] = c;
+      a.flags[r] = static_cast<uint64_t>(c) + 1;
+    }
+    if (row + gridDim.x < a.nrows) __syncthreads();  // the next row reuses the shared arrays
   }
 }
 
@@ -314,7 +345,10 @@ static int fused_vpt(int64_t vin, int max_vpt) {
   return 0;
 }
 
-static int fused_hist(const Sizes &s) { return s.T > 0 ? (s.E + s.T - 1) / s.T : s.E; }
+static int fused_hist(const Sizes &s) {
+  const int rows = s.T < kFusedHistRows ? s.T : kFusedHistRows;
+  return rows > 0 ? (s.E + rows - 1) / rows : s.E;
+}
 
 // Whether the batch runs as the one fused kernel (rows of at most 16 KiB).
 static bool fused_fits(const Sizes &s) {
