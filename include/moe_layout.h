@@ -44,11 +44,14 @@
  *   - One step is moe_layout -> moe_dispatch -> (the caller's experts) ->
  *     moe_combine, in stream order on one stream.
  *   - The kernels use programmatic dependent launch: each may be scheduled
- *     while the kernel before it in the stream finishes, and waits for that
- *     kernel's results before touching them. moe_dispatch starts reading x (an
- *     input that moe_layout never writes) before that wait, so x must be
- *     complete before moe_layout is enqueued (as it is when x comes from a copy
- *     or a kernel enqueued earlier).
+ *     while the kernel before it in the stream is still running, and waits for
+ *     that kernel to complete (griddepcontrol.wait) before it reads anything.
+ *     So every input may be written by the kernel enqueued immediately before
+ *     the call. The one exception is moe_dispatch, which starts loading x
+ *     before its wait (in a step the kernel before it is moe_layout, which
+ *     never writes x): x must not be written by the kernel enqueued
+ *     immediately before moe_dispatch. moe_layout_dispatch reads nothing
+ *     before its wait.
  */
 #ifndef MOE_LAYOUT_H
 #define MOE_LAYOUT_H
@@ -139,18 +142,23 @@ moe_status moe_layout(const moe_desc *desc, const int32_t *topk_idx, int32_t *co
  *   recv_meta [E][R][max_m][4] int32, 16-byte
  *   aligned (written; only slots pos < count are touched).
  * Device errors: a flag still zero after the bounded wait -> MOE_ETIMEOUT;
- * tok_slot out of range -> MOE_EINVAL; the affected copies are skipped. */
+ * tok_slot out of range -> MOE_EINVAL; the affected copies are skipped.
+ * x is loaded before the dependency wait (its loads overlap moe_layout's
+ * tail), so it must not be written by the kernel enqueued immediately before
+ * this call; x_scales and the rest are read after the wait. */
 moe_status moe_dispatch(const moe_desc *desc, const void *x, const float *x_scales, const int32_t *tok_slot,
                         const uint64_t *flags, void *recv_x, float *recv_scales, int32_t *recv_meta,
                         int32_t *err, void *stream);
 
 /* Layout and dispatch in one call: the same outputs as moe_layout followed by
  * moe_dispatch (same arguments, same device errors except that no flag wait
- * can time out). When one CTA can hold a source rank's per-expert token
- * bitmaps (T <= 1024, rows of at most 16 KiB) it runs as one kernel in which
- * every CTA computes its rows' slots itself while their bulk loads are in
- * flight (Perplexity, "Dispatch": the counting warp beside the packing warps);
- * otherwise it launches the two kernels. */
+ * can time out). For decode-sized batches (T <= 1024 tokens per rank, input
+ * rows of at most 16 KiB) it runs as one kernel in which every CTA computes
+ * the token-order slots of its row itself, from its rank's routing, while the
+ * row's loads are in flight (Perplexity, "Dispatch": the counting warp beside
+ * the packing warps); otherwise it launches the two kernels. Reads nothing
+ * before its dependency wait, so x, x_scales and topk_idx may come from the
+ * kernel enqueued immediately before it. */
 moe_status moe_layout_dispatch(const moe_desc *desc, const int32_t *topk_idx, const void *x, const float *x_scales,
                                int32_t *counts, uint64_t *flags, int32_t *tok_slot, void *recv_x,
                                float *recv_scales, int32_t *recv_meta, int32_t *err, void *stream);
