@@ -93,7 +93,8 @@ REASON_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 100 ms) while the GPU works."""
+    """nvidia-smi samples (every 20 ms) from before the warm-up steps to after the
+    last measurement (the per-config steps and the end-to-end pass included)."""
 
     def __init__(self, local_rank: int):
         vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -101,18 +102,20 @@ class ClockSampler:
         self.samples = []
         self.proc = None
         self.thread = None
+        self.t0 = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.gpu, f"--query-gpu={','.join(CLOCK_FIELDS)}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
             return self
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        self.t0 = time.time()
         return self
 
     def _read(self):
@@ -137,13 +140,16 @@ class ClockSampler:
             except ValueError:
                 return None
 
-        busy = [s for s in self.samples if (num(s[3]) or 0) > 0] or self.samples
+        busy_only = [s for s in self.samples if (num(s[3]) or 0) > 0]
+        busy = busy_only or self.samples
         sm = [num(s[0]) for s in busy if num(s[0]) is not None]
         mx = [num(s[1]) for s in self.samples if num(s[1]) is not None]
         reasons = sorted({REASON_NAMES[i] for s in busy for i in range(4) if s[4 + i].lower() == "active"})
         power = [num(s[2]) for s in busy if num(s[2]) is not None]
+        window = round(time.time() - self.t0, 2) if self.t0 is not None else None
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.samples), "busy_samples": len(busy) if sm else 0,
+                "window_s": window, "interval_ms": 20,
+                "reasons": reasons, "samples": len(self.samples), "busy_samples": len(busy_only),
                 "power_w_max": max(power) if power else None}
 
 
@@ -179,6 +185,100 @@ def profiled_traffic(kernel_file: str, workload: str):
 
 
 # --- native arm -------------------------------------------------------------------
+
+# Throughput configs reported beside the headline workload (the benchmark spec's
+# prefill target and the other large shapes).
+PER_CONFIG = ("ds_prefill", "mixtral", "skewed")
+
+
+def time_config(name, K, W, num_sms, dev, flush, world):
+    """K steps (fused layout+dispatch call -> combine) of one more workload on its
+    own buffers, timed like the headline step: L2 flushed before each step
+    outside the events, CUDA events on the launching stream, max over ranks."""
+    import torch
+
+    from combine_moe_layout_gb300 import _binding as B
+    from combine_moe_layout_gb300 import pipeline as P
+    from combine_moe_layout_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[name]
+    desc = B.MoeDesc.of(w, num_sms)
+    need = sum(B.moe_buffer_sizes(desc).values()) + 3 * w.num_tokens * w.in_row_bytes + (2 << 30)
+    free = torch.cuda.mem_get_info(dev)[0]
+    if free < need:
+        return {"unavailable": f"needs {need / 2**30:.1f} GiB of device memory, {free / 2**30:.1f} GiB free"}
+    inp = wl.make_inputs(w)
+    step = P.MoeStep(w, dev, num_sms)
+    d = P.to_device(inp, dev)
+    stream = torch.cuda.current_stream()
+    step.reset()
+    step.run(d, fused=True)  # the synthetic experts once; their outputs stay resident
+    if step.error() != B.MOE_OK:
+        raise RuntimeError(f"{name}: first step failed")
+    for _ in range(W):
+        flush()
+        step.layout_dispatch(d)
+        step.combine(d)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    torch.cuda.synchronize()
+    barrier(world)
+    for i in range(K):
+        flush()
+        ev[i][0].record(stream)
+        step.layout_dispatch(d)
+        step.combine(d)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    for i in range(K):  # per kernel: events between the two calls
+        flush()
+        ev[i][0].record(stream)
+        step.layout_dispatch(d)
+        ev[i][1].record(stream)
+        step.combine(d)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if step.error() != B.MOE_OK:
+        raise RuntimeError(f"{name}: timed steps latched an error")
+    kern = {"layout_dispatch": statistics.mean(a.elapsed_time(b) for a, b, _ in ev),
+            "combine": statistics.mean(b.elapsed_time(c) for _, b, c in ev)}
+    job = whole_job(w.num_tokens, sum(step_ms), K, world, dev)
+    ab = dict(w.algorithmic_bytes())
+    ab["layout_dispatch"] = ab["layout"] + ab["dispatch"]
+    peak, peak_kind = measured_hbm_peak()
+    step_s = job["ms_per_step"] / 1e3
+    kernels = {}
+    for kname, ms in kern.items():
+        gbs = ab[kname] / (ms / 1e3) / 1e9
+        kernels[kname] = {"us": round(ms * 1e3, 2), "algorithmic_bytes": ab[kname], "GBps": round(gbs, 1),
+                          "frac_of_measured_hbm": round(gbs / peak, 4)}
+    dom = max(kernels, key=lambda kk: kernels[kk]["us"])
+    nk = B.moe_layout_dispatch_kernels(step.desc)
+    out = {
+        "description": wl.DESCRIPTIONS[name],
+        "tokens_per_step": w.num_tokens,
+        "us_per_step": round(job["ms_per_step"] * 1e3, 2),
+        "tokens_per_s": round(job["value"], 1),
+        "algorithmic_bytes_per_step": ab["total"],
+        "step_GBps": round(ab["total"] / step_s / 1e9, 1),
+        "frac_of_measured": round(ab["total"] / step_s / 1e9 / peak, 4),
+        "frac_of_8TBps": round(ab["total"] / step_s / 1e9 / NOMINAL_HBM_GBS, 4),
+        "step_kernels": ("fused layout+dispatch kernel, combine" if nk == 1 else
+                         "layout+dispatch call (a layout kernel, then the dispatch kernel), combine"),
+        "kernels": kernels,
+        "roofline": {"kernel": "combine_kernel" if dom == "combine" else "layout+dispatch", "bound": "hbm",
+                     "achieved": kernels[dom]["GBps"], "peak": peak, "peak_kind": f"{peak_kind} (copy bandwidth)",
+                     "unit": "GB/s", "frac": kernels[dom]["frac_of_measured_hbm"],
+                     "traffic": profiled_traffic("moe_combine.cu", name) if dom == "combine" else None,
+                     "algorithmic_bytes_per_launch": ab[dom]},
+        "gpu_launches": (nk + 1) * K,
+        "steps": K,
+    }
+    del step, d
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
 
 def run_native(args, rank, local_rank, world):
     import numpy as np
@@ -244,6 +344,7 @@ def run_native(args, rank, local_rank, world):
             step.combine(dd, out=out)
 
     K, W = args.steps, args.warmup
+    sampler = ClockSampler(local_rank).start()
     for _ in range(W):
         flush()
         path(d)
@@ -263,7 +364,6 @@ def run_native(args, rank, local_rank, world):
             timed()
         torch.cuda.synchronize()
 
-    sampler = ClockSampler(local_rank).start()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     torch.cuda.synchronize()
     barrier(world)
@@ -293,6 +393,13 @@ def run_native(args, rank, local_rank, world):
             kev[i][j + 1].record(stream)
     torch.cuda.synchronize()
     kern_ms = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in kev) for j, (name, _) in enumerate(stages)}
+
+    # the other throughput configs, each timed the same way on its own buffers (freed after)
+    per_config = {}
+    if not (args.no_per_config or args.packed or args.graph or args.unfused):
+        for name in PER_CONFIG:
+            if name != w.name:
+                per_config[name] = time_config(name, K, W, args.num_sms, dev, flush, world)
 
     # end to end: the step's inputs packed in one pinned host buffer, copied in
     # with one H2D copy, and the output read back, all inside the timed region
@@ -532,8 +639,9 @@ def run_native(args, rank, local_rank, world):
                      "algorithmic_bytes_per_launch": ab[comb]},
         "kernels": kernel_stats,
         "kernel_timing": "CUDA events between the launches, a second pass of the same K steps",
+        "per_config": per_config,
         "e2e": e2e,
-        "gpu_launches": kernels * K,
+        "gpu_launches": kernels * K + sum(c.get("gpu_launches", 0) for c in per_config.values()),
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world >= 1:
@@ -620,12 +728,12 @@ def run_expert(args, rank, local_rank, world):
         flush_r.sum()
 
     K, W = args.steps, args.warmup
+    sampler = ClockSampler(local_rank).start()
     for _ in range(W):
         flush()
         path(d)
     torch.cuda.synchronize()
     barrier(world)
-    sampler = ClockSampler(local_rank).start()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for i in range(K):
         flush()
@@ -999,6 +1107,8 @@ def main(argv=None):
                          "dispatch overlapping the previous step's combine; pipelined-copy = pipelined with "
                          "combine writing to device memory and a copy engine moving the output out")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip timing the other throughput configs (ds_prefill, mixtral, skewed)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)
     if args.workload is None:

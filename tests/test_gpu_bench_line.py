@@ -55,14 +55,38 @@ def _check_common(j):
 
 def test_dispatch_combine_line():
     require_gpu()
-    j = _line()
+    j = _line("--no-per-config")
     _check_common(j)
     assert j["unit"] == "tokens/s" and j["roofline"]["bound"] == "hbm" and j["roofline"]["unit"] == "GB/s"
     assert j["gpu_launches"] == 2 * 3  # the fused layout+dispatch kernel and combine, per timed step
+    assert j["per_config"] == {}
+    assert j["clocks"]["samples"] >= 1 and j["clocks"]["interval_ms"] == 20
+
+
+def test_dispatch_combine_line_with_the_other_configs():
+    """The same line with ds_prefill, mixtral and skewed timed beside the headline
+    workload: each entry has its step time, throughput, HBM fractions, per-kernel
+    times and the roofline of its dominant kernel (or says why it could not run)."""
+    require_gpu()
+    j = _line("--no-e2e")
+    assert set(j["per_config"]) == {"ds_prefill", "mixtral", "skewed"}
+    launches = 2 * 3
+    for name, c in j["per_config"].items():
+        if "unavailable" in c:
+            continue
+        for key in ("us_per_step", "tokens_per_s", "step_GBps", "frac_of_measured", "frac_of_8TBps", "kernels",
+                    "roofline", "step_kernels"):
+            assert key in c, (name, key)
+        assert c["us_per_step"] > 0 and c["tokens_per_s"] > 0 and c["steps"] == 3
+        r = c["roofline"]
+        assert r["bound"] == "hbm" and r["achieved"] > 0 and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+        assert set(c["kernels"]) == {"layout_dispatch", "combine"}
+        launches += c["gpu_launches"]
+    assert j["gpu_launches"] == launches
 
 
 def test_expert_step_line():
     require_gpu()
-    j = _line("--expert")
+    j = _line("--expert", "--no-per-config")
     _check_common(j)
     assert j["unit"] == "tokens/s"
