@@ -7,8 +7,8 @@
 // other warps pack the tokens; "NVSHMEM and DeepEP: GPU-initiated
 // communication", low-latency section: fixed slots, no exchange). Every CTA is
 // such a sender for one row (src, t) at a time:
-//   1. all threads load the row into registers (32-byte vectors where the
-//      rows allow, else 16-byte ones), its scales and the row's k experts;
+//   1. all threads load the row into registers (16- or 32-byte vectors), its
+//      scales and the row's k experts;
 //   2. the CTA reads the routing entries of rank src's earlier tokens
 //      (L2-resident after the first CTA) and, per thread, counts the entries
 //      equal to each of the row's k experts; warp reductions and one exchange
@@ -35,6 +35,7 @@ constexpr int kFusedWarps = kFusedThreads / 32;
 constexpr int kFusedMaxTokens = 1024;
 constexpr int kFusedMaxVec16 = 8;  // 16-byte vectors per thread: rows of at most 128 * 8 * 16 B = 16 KiB
 constexpr int kFusedMaxVec32 = 4;  // 32-byte vectors per thread: the same 16 KiB
+constexpr int64_t kFusedNarrowMaxRow = 8192;  // plain copies of rows up to this many bytes use 16-byte vectors
 constexpr int kFusedMaxHist = 2048;       // experts one CTA histograms (G = ceil(E / T))
 constexpr int kFusedScanRegs = 2;        // int4 routing loads per thread issued with the row's loads
 constexpr int kFusedHistRows = 32;       // rows per rank that also count experts for counts and flags
@@ -60,8 +61,7 @@ struct FusedArgs {
 };
 
 // A W-byte piece of a row (W = 16 or 32), moved with one vector load and one
-// vector store per slot. 32-byte stores measured ~8 TB/s of writes on GB300
-// against ~5.5 TB/s for 16-byte ones, at the 60 MB a decode dispatch writes.
+// vector store per slot.
 template <int W>
 struct RowVec {
   uint32_t w[W / 4];
@@ -385,14 +385,24 @@ static moe_status launch_fused(const FusedArgs &a, int sms, cudaStream_t stream)
 }
 
 template <int KC, bool QUANT>
-static moe_status launch_fused_w(const FusedArgs &a, bool wide, int sms, cudaStream_t stream) {
-  if (!wide) return launch_fused<16, kFusedMaxVec16, kMaxTopk, QUANT>(a, sms, stream);
-  switch (fused_vpt(a.vin, kFusedMaxVec32)) {
-    case 1: return launch_fused<32, 1, KC, QUANT>(a, sms, stream);
-    case 2: return launch_fused<32, 2, KC, QUANT>(a, sms, stream);
-    case 4: return launch_fused<32, 4, KC, QUANT>(a, sms, stream);
-    default: return MOE_EINVAL;
+static moe_status launch_fused_w(const FusedArgs &a, int width, int sms, cudaStream_t stream) {
+  if (width == 32) {
+    switch (fused_vpt(a.vin, kFusedMaxVec32)) {
+      case 1: return launch_fused<32, 1, KC, QUANT>(a, sms, stream);
+      case 2: return launch_fused<32, 2, KC, QUANT>(a, sms, stream);
+      case 4: return launch_fused<32, 4, KC, QUANT>(a, sms, stream);
+      default: return MOE_EINVAL;
+    }
   }
+  if constexpr (!QUANT) {
+    switch (fused_vpt(a.vin, kFusedMaxVec16)) {
+      case 1: return launch_fused<16, 1, KC, false>(a, sms, stream);
+      case 2: return launch_fused<16, 2, KC, false>(a, sms, stream);
+      case 4: return launch_fused<16, 4, KC, false>(a, sms, stream);
+      default: break;
+    }
+  }
+  return launch_fused<16, 8, kMaxTopk, QUANT>(a, sms, stream);  // rows whose pointers allow only 16 bytes
 }
 
 moe_status launch_layout_dispatch(const Sizes &s, const int32_t *topk_idx, const void *x, const float *x_scales,
@@ -404,9 +414,14 @@ moe_status launch_layout_dispatch(const Sizes &s, const int32_t *topk_idx, const
     if (st != MOE_OK || s.ntok == 0) return st;
     return launch_dispatch(s, x, x_scales, tok_slot, flags, recv_x, recv_scales, recv_meta, err, num_sms, stream);
   }
-  // 32-byte vectors when the input rows and (copy mode) the slot rows allow them
-  const bool wide = s.in_row_bytes % 32 == 0 && aligned32(x) &&
-                    (s.quant || (s.row_bytes % 32 == 0 && aligned32(recv_x)));
+  // Vector width, measured on GB300: plain copies of rows up to 8 KiB are
+  // fastest with 16-byte vectors (ds_decode step 36.6 vs 37.6 us with 32-byte
+  // ones), longer rows and quantised rows with 32-byte vectors (skewed 162.3
+  // vs 163.4 us; ds_decode with bf16 rows 46.1 vs 56.6 us), where the rows and
+  // pointers allow them.
+  const bool can32 = s.in_row_bytes % 32 == 0 && aligned32(x) &&
+                     (s.quant || (s.row_bytes % 32 == 0 && aligned32(recv_x)));
+  const bool wide = can32 && (s.quant || s.in_row_bytes > kFusedNarrowMaxRow);
   FusedArgs a{};
   a.topk_idx = topk_idx;
   a.counts = counts;
@@ -433,10 +448,11 @@ moe_status launch_layout_dispatch(const Sizes &s, const int32_t *topk_idx, const
   a.in_row_bytes = static_cast<uint32_t>(s.in_row_bytes);
   a.nrows = s.ntok;
   const int sms = num_sms > 0 && num_sms < sm_count() ? num_sms : sm_count();
+  const int width = wide ? 32 : 16;
   if (s.k <= 8)
-    return s.quant ? launch_fused_w<8, true>(a, wide, sms, stream) : launch_fused_w<8, false>(a, wide, sms, stream);
-  return s.quant ? launch_fused_w<kMaxTopk, true>(a, wide, sms, stream)
-                 : launch_fused_w<kMaxTopk, false>(a, wide, sms, stream);
+    return s.quant ? launch_fused_w<8, true>(a, width, sms, stream) : launch_fused_w<8, false>(a, width, sms, stream);
+  return s.quant ? launch_fused_w<kMaxTopk, true>(a, width, sms, stream)
+                 : launch_fused_w<kMaxTopk, false>(a, width, sms, stream);
 }
 
 }  // namespace moe
