@@ -41,6 +41,21 @@ class MoeSizes(ctypes.Structure):
                 ("recv_x", "recv_scales", "recv_meta", "counts", "flags", "tok_slot", "expert_out")]
 
 
+MOE_MAX_PARTS = 8
+
+
+class MoeParts(ctypes.Structure):
+    """The receive side in G parts (moe_parts of include/moe_layout.h)."""
+    _fields_ = [
+        ("num_parts", ctypes.c_int32),
+        ("recv_x", ctypes.c_void_p * MOE_MAX_PARTS),
+        ("recv_scales", ctypes.c_void_p * MOE_MAX_PARTS),
+        ("recv_meta", ctypes.c_void_p * MOE_MAX_PARTS),
+        ("flags", ctypes.c_void_p * MOE_MAX_PARTS),
+        ("expert_out", ctypes.c_void_p * MOE_MAX_PARTS),
+    ]
+
+
 class MoeError(RuntimeError):
     def __init__(self, status: int, what: str):
         super().__init__(f"{what}: {moe_status_string(status)} (status {status})")
@@ -83,6 +98,11 @@ def _open(path: str):
     lib.moe_expert_down_fp8.argtypes = [pdesc, ctypes.c_int32] + [vp] * 8
     lib.moe_combine.argtypes = [pdesc] + [vp] * 7
     lib.moe_reset.argtypes = [pdesc] + [vp] * 3
+    pparts = ctypes.POINTER(MoeParts)
+    lib.moe_layout_dispatch_parts.argtypes = [pdesc, vp, vp, vp, vp, vp, pparts, vp, vp]
+    lib.moe_combine_parts.argtypes = [pdesc, pparts, vp, vp, vp, vp, vp]
+    lib.moe_expert_stub_parts.argtypes = [pdesc, pparts, vp, vp, vp]
+    lib.moe_reset_parts.argtypes = [pdesc, pparts, vp, vp]
     lib.moe_get_error.argtypes = [vp, vp]
     lib.moe_layout_dispatch_kernels.argtypes = [pdesc]
     lib.moe_layout_dispatch_kernels.restype = ctypes.c_int32
@@ -91,8 +111,8 @@ def _open(path: str):
     for name in ("moe_buffer_sizes", "moe_layout", "moe_dispatch", "moe_layout_dispatch", "moe_dispatch_recv",
                  "moe_expert_stub", "moe_combine", "moe_combine_packed", "moe_route_stats", "moe_reset",
                  "moe_expert_gate_up", "moe_expert_down", "moe_expert_mlp_noalloc", "moe_expert_gate_up_fp8",
-                 "moe_expert_down_fp8", "moe_expert_mlp_noalloc_fp8",
-                 "moe_get_error"):
+                 "moe_expert_down_fp8", "moe_expert_mlp_noalloc_fp8", "moe_layout_dispatch_parts",
+                 "moe_combine_parts", "moe_expert_stub_parts", "moe_reset_parts", "moe_get_error"):
         getattr(lib, name).restype = st
     return lib
 
@@ -228,6 +248,29 @@ def moe_reset(desc, flags, err, stream=None):
     _check(load().moe_reset(ctypes.byref(desc), _ptr(flags), _ptr(err), _stream(stream)), "moe_reset")
 
 
+def moe_layout_dispatch_parts(desc, topk_idx, x, x_scales, counts, tok_slot, parts: "PartBuffers", err,
+                              stream=None):
+    _check(load().moe_layout_dispatch_parts(ctypes.byref(desc), _ptr(topk_idx, True), _ptr(x, True),
+                                            _ptr(x_scales, True), _ptr(counts), _ptr(tok_slot),
+                                            ctypes.byref(parts.table()), _ptr(err), _stream(stream)),
+           "moe_layout_dispatch_parts")
+
+
+def moe_combine_parts(desc, parts: "PartBuffers", topk_weights, tok_slot, out, err, stream=None):
+    _check(load().moe_combine_parts(ctypes.byref(desc), ctypes.byref(parts.table()), _ptr(topk_weights, True),
+                                    _ptr(tok_slot), _ptr(out, True), _ptr(err), _stream(stream)), "moe_combine_parts")
+
+
+def moe_expert_stub_parts(desc, parts: "PartBuffers", counts, err, stream=None):
+    _check(load().moe_expert_stub_parts(ctypes.byref(desc), ctypes.byref(parts.table()), _ptr(counts), _ptr(err),
+                                        _stream(stream)), "moe_expert_stub_parts")
+
+
+def moe_reset_parts(desc, parts: "PartBuffers", err, stream=None):
+    _check(load().moe_reset_parts(ctypes.byref(desc), ctypes.byref(parts.table()), _ptr(err), _stream(stream)),
+           "moe_reset_parts")
+
+
 def moe_get_error(err, stream=None) -> int:
     """Synchronise, read and clear the device error word; returns its status code."""
     return int(load().moe_get_error(_ptr(err), _stream(stream)))
@@ -294,4 +337,59 @@ def allocate_buffers(desc: MoeDesc, device, with_expert_out: bool | None = None)
         expert_out=expert_out,
         out=torch.empty((R, T, H), dtype=torch.bfloat16, device=dev),
         err=torch.zeros(1, dtype=torch.int32, device=dev),
+    )
+
+
+@dataclass
+class PartBuffers:
+    """The receive side in G parts: part g holds the regions of ranks
+    [g*R/G, (g+1)*R/G), every buffer 1/G of moe_buffer_sizes' size."""
+    recv_x: list
+    recv_scales: list | None
+    recv_meta: list
+    flags: list
+    expert_out: list | None
+
+    @property
+    def num_parts(self) -> int:
+        return len(self.recv_x)
+
+    def table(self) -> MoeParts:
+        t = MoeParts()
+        t.num_parts = self.num_parts
+        for g in range(self.num_parts):
+            t.recv_x[g] = _ptr(self.recv_x[g]).value
+            t.recv_meta[g] = _ptr(self.recv_meta[g]).value
+            t.flags[g] = _ptr(self.flags[g]).value
+            if self.recv_scales is not None:
+                t.recv_scales[g] = _ptr(self.recv_scales[g]).value
+            if self.expert_out is not None:
+                t.expert_out[g] = _ptr(self.expert_out[g]).value
+        return t
+
+
+def allocate_parts(desc: MoeDesc, num_parts: int, device, with_expert_out: bool | None = None,
+                   alloc=None) -> PartBuffers:
+    """Separate allocations for each part of the receive side. alloc(shape,
+    dtype) makes one buffer (default torch.empty on the device)."""
+    R, H, E, M = desc.num_ranks, desc.hidden, desc.num_experts, desc.max_m
+    if num_parts < 1 or num_parts > MOE_MAX_PARTS or R % num_parts:
+        raise ValueError("num_parts must divide the ranks and be at most MOE_MAX_PARTS")
+    dev = torch.device(device)
+    if alloc is None:
+        def alloc(shape, dtype):
+            return torch.empty(shape, dtype=dtype, device=dev)
+    slots = E * R * M // num_parts
+    regions = E * R // num_parts
+    fp8 = desc.dtype != MOE_BF16
+    row = H if fp8 else 2 * H
+    if with_expert_out is None:
+        with_expert_out = fp8
+    G = range(num_parts)
+    return PartBuffers(
+        recv_x=[alloc((slots, row), torch.uint8) for _ in G],
+        recv_scales=[alloc((slots, H // 128), torch.float32) for _ in G] if fp8 else None,
+        recv_meta=[alloc((slots, 4), torch.int32) for _ in G],
+        flags=[alloc((regions,), torch.int64) for _ in G],
+        expert_out=[alloc((slots, H), torch.bfloat16) for _ in G] if with_expert_out else None,
     )

@@ -30,15 +30,27 @@ namespace moe {
 constexpr int kCombineThreads = 128;
 
 struct CombineArgs {
-  const uint16_t *y;
+  SlotParts parts;  // the expert outputs y (rows of H) and the count + 1 flags, per part
   const float *weights;
   const int32_t *tok_slot;
-  uint64_t *flags;
   uint16_t *out;
   int32_t *err;
-  int H, k, nflags, chunks, early;
+  int H, k, chunks, early;
   int64_t nslots;  // rows of y: the slots (fixed-slot layout) or the packed rows
 };
+
+// Row `slot` of y, in its part.
+__device__ __forceinline__ const uint16_t *y_row(const CombineArgs &a, int32_t slot) {
+  int g;
+  const int64_t l = slot_local(a.parts, slot, &g);
+  return a.parts.y[g] + l * a.H;
+}
+
+// Block b < G clears part b's count + 1 flags.
+__device__ __forceinline__ void clear_flags(const CombineArgs &a, int64_t b) {
+  if (b < a.parts.G)
+    for (int i = threadIdx.x; i < a.parts.regions_per_part; i += blockDim.x) a.parts.flags[b][i] = 0;
+}
 
 __device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float w, const uint4 &v) {
   const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -94,8 +106,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_tma_kernel(CombineArg
   }
   grid_dependency_wait();
   if (a.early) grid_dependents_launch();
-  if (b == 0)
-    for (int i = tid; i < a.nflags; i += blockDim.x) a.flags[i] = 0;
+  clear_flags(a, b);
   if (tid < K) {
     int32_t slot = __ldg(a.tok_slot + tok * K + tid);
     float w = __ldg(a.weights + tok * K + tid);
@@ -115,7 +126,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_tma_kernel(CombineArg
     mbar_arrive_expect_tx(&bar, nvalid * bytes);
     for (int j = 0; j < K; ++j)
       if (s_slot[j] >= 0)
-        bulk_load(&stage[j][0], a.y + static_cast<int64_t>(s_slot[j]) * a.H + static_cast<int64_t>(v0) * 8, bytes,
+        bulk_load(&stage[j][0], y_row(a, s_slot[j]) + static_cast<int64_t>(v0) * 8, bytes,
                   &bar);
   }
   if (!mbar_wait_bounded(&bar, 0)) {
@@ -149,8 +160,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
 
   grid_dependency_wait();
   if (a.early) grid_dependents_launch();
-  if (b == 0)
-    for (int i = threadIdx.x; i < a.nflags; i += blockDim.x) a.flags[i] = 0;
+  clear_flags(a, b);
 
   // this token's slots and weights (the same for the whole warp: broadcast loads)
   int32_t slot[KC];
@@ -176,7 +186,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
     for (int j = 0; j < KC; ++j)
       if (j < k)
         y[u][j] = (v < V && slot[j] >= 0)
-                      ? __ldcs(reinterpret_cast<const uint4 *>(a.y + static_cast<int64_t>(slot[j]) * a.H) + v)
+                      ? __ldcs(reinterpret_cast<const uint4 *>(y_row(a, slot[j])) + v)
                       : make_uint4(0, 0, 0, 0);
   }
   uint4 *dst = reinterpret_cast<uint4 *>(a.out + tok * a.H);
@@ -219,14 +229,15 @@ moe_status launch_combine_k(CombineArgs a, int64_t ntok, cudaStream_t stream) {
   return launch_status();
 }
 
-moe_status launch_combine(const Sizes &s, const uint16_t *y, int64_t y_rows, const float *weights,
-                          const int32_t *tok_slot, uint64_t *flags, uint16_t *out, int32_t *err,
-                          cudaStream_t stream) {
-  CombineArgs a{y, weights, tok_slot, flags, out, err, s.H, s.k, s.E * s.R, 1, early_trigger(s.ntok), y_rows};
+moe_status launch_combine(const Sizes &s, const SlotParts &parts, int64_t y_rows, const float *weights,
+                          const int32_t *tok_slot, uint16_t *out, int32_t *err, cudaStream_t stream) {
+  CombineArgs a{parts, weights, tok_slot, out, err, s.H, s.k, 1, early_trigger(s.ntok), y_rows};
   if (s.ntok == 0) {
     // nothing to gather; still clear the flags for the next step
-    if (cudaMemsetAsync(flags, 0, static_cast<size_t>(s.E) * s.R * sizeof(uint64_t), stream) != cudaSuccess)
-      return MOE_ECUDA;
+    for (int g = 0; g < parts.G; ++g)
+      if (cudaMemsetAsync(parts.flags[g], 0, static_cast<size_t>(parts.regions_per_part) * sizeof(uint64_t),
+                          stream) != cudaSuccess)
+        return MOE_ECUDA;
     return MOE_OK;
   }
   switch (s.k) {
@@ -255,8 +266,8 @@ extern "C" moe_status moe_combine(const moe_desc *desc, const uint16_t *expert_o
   if (!aligned16(expert_out) || !aligned16(out) || !aligned4(topk_weights) || !aligned4(tok_slot) ||
       !aligned4(err) || (reinterpret_cast<uintptr_t>(flags) & 7u) != 0)
     return MOE_EINVAL;
-  return launch_combine(s, expert_out, s.nslots, topk_weights, tok_slot, flags, out, err,
-                        static_cast<cudaStream_t>(stream));
+  return launch_combine(s, single_part(s, nullptr, nullptr, nullptr, flags, expert_out), s.nslots, topk_weights,
+                        tok_slot, out, err, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" moe_status moe_combine_packed(const moe_desc *desc, const uint16_t *packed_y, const int32_t *tok_packed,
@@ -271,6 +282,20 @@ extern "C" moe_status moe_combine_packed(const moe_desc *desc, const uint16_t *p
   if (!aligned16(packed_y) || !aligned16(out) || !aligned4(topk_weights) || !aligned4(tok_packed) ||
       !aligned4(err) || (reinterpret_cast<uintptr_t>(flags) & 7u) != 0)
     return MOE_EINVAL;
-  return launch_combine(s, packed_y, s.ntok * s.k, topk_weights, tok_packed, flags, out, err,
-                        static_cast<cudaStream_t>(stream));
+  return launch_combine(s, single_part(s, nullptr, nullptr, nullptr, flags, packed_y), s.ntok * s.k, topk_weights,
+                        tok_packed, out, err, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" moe_status moe_combine_parts(const moe_desc *desc, const moe_parts *parts, const float *topk_weights,
+                                        const int32_t *tok_slot, uint16_t *out, int32_t *err, void *stream) {
+  Sizes s;
+  moe_status st = check_desc(desc, &s);
+  if (st != MOE_OK) return st;
+  SlotParts p;
+  st = parts_from(s, parts, false, s.ntok > 0, &p);
+  if (st != MOE_OK) return st;
+  if (err == nullptr) return MOE_EINVAL;
+  if (s.ntok > 0 && (topk_weights == nullptr || tok_slot == nullptr || out == nullptr)) return MOE_EINVAL;
+  if (!aligned16(out) || !aligned4(topk_weights) || !aligned4(tok_slot) || !aligned4(err)) return MOE_EINVAL;
+  return launch_combine(s, p, s.nslots, topk_weights, tok_slot, out, err, static_cast<cudaStream_t>(stream));
 }

@@ -173,6 +173,53 @@ __device__ __forceinline__ void quantize_blocks(const uint16_t *src, uint8_t *ds
 }
 
 // ---------------------------------------------------------------------------
+// Slot partitions: the fixed-slot buffers (rows, scales, headers, count+1
+// flags, expert outputs) split into G parts as G GPUs of an EP group would hold
+// them. Part g holds the regions of ranks [g*R/G, (g+1)*R/G): global slots
+// [g*P, (g+1)*P) at local slot s - g*P, with P = (R/G)*L*R*max_m, and regions
+// likewise. Slot ids (tok_slot, headers) stay global. G = 1 is the single
+// buffer; its address arithmetic takes a uniform branch and no division.
+// ---------------------------------------------------------------------------
+constexpr int kMaxParts = MOE_MAX_PARTS;
+
+struct SlotParts {
+  int G;
+  int32_t slots_per_part;    // P
+  int32_t regions_per_part;  // P / max_m
+  uint8_t *recv_x[kMaxParts];
+  float *recv_scales[kMaxParts];
+  int4 *recv_meta[kMaxParts];
+  uint64_t *flags[kMaxParts];
+  uint16_t *y[kMaxParts];  // expert outputs (bf16 rows of H)
+};
+
+// Part and local index of a global slot (or region, with per = regions_per_part).
+// Slot ids fit in 32 bits (the desc check bounds E*R*max_m), so 32-bit division.
+__device__ __forceinline__ int part_split(int G, int32_t per, int64_t id, int64_t *local) {
+  if (G == 1) {
+    *local = id;
+    return 0;
+  }
+  const uint32_t u = static_cast<uint32_t>(id);
+  const uint32_t g = u / static_cast<uint32_t>(per);
+  *local = static_cast<int64_t>(u - g * static_cast<uint32_t>(per));
+  return static_cast<int>(g);
+}
+
+// Local slot of a global slot, and its part in *g.
+__device__ __forceinline__ int64_t slot_local(const SlotParts &p, int64_t slot, int *g) {
+  int64_t l;
+  *g = part_split(p.G, p.slots_per_part, slot, &l);
+  return l;
+}
+
+__device__ __forceinline__ uint64_t *flag_ptr(const SlotParts &p, int64_t region) {
+  int64_t l;
+  const int g = part_split(p.G, p.regions_per_part, region, &l);
+  return p.flags[g] + l;
+}
+
+// ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
 struct Sizes {
@@ -260,10 +307,59 @@ __host__ __device__ inline int64_t inflight_end(int64_t i, int64_t S, int64_t n)
   return end < n ? end : n;
 }
 
-moe_status launch_layout(const Sizes &s, const int32_t *topk_idx, int32_t *counts, uint64_t *flags,
+// One buffer of each kind: the parts of a single-device step.
+inline SlotParts single_part(const Sizes &s, void *recv_x, float *recv_scales, int32_t *recv_meta, uint64_t *flags,
+                             const void *y) {
+  SlotParts p{};
+  p.G = 1;
+  p.slots_per_part = static_cast<int32_t>(s.nslots);
+  p.regions_per_part = s.E * s.R;
+  p.recv_x[0] = static_cast<uint8_t *>(recv_x);
+  p.recv_scales[0] = recv_scales;
+  p.recv_meta[0] = reinterpret_cast<int4 *>(recv_meta);
+  p.flags[0] = flags;
+  p.y[0] = static_cast<uint16_t *>(const_cast<void *>(y));
+  return p;
+}
+
+// The internal part table of a caller's moe_parts, checked: G divides R and is
+// at most kMaxParts; the buffers each use are present and aligned (recv: rows,
+// scales, headers and flags; y: expert outputs; flags are always needed).
+inline moe_status parts_from(const Sizes &s, const moe_parts *p, bool need_recv, bool need_y, SlotParts *out) {
+  if (p == nullptr) return MOE_EINVAL;
+  const int G = p->num_parts;
+  if (G < 1 || G > kMaxParts || s.R % G != 0) return MOE_EINVAL;
+  SlotParts q{};
+  q.G = G;
+  q.slots_per_part = static_cast<int32_t>(s.nslots / G);
+  q.regions_per_part = s.E * s.R / G;
+  for (int g = 0; g < G; ++g) {
+    if (p->flags[g] == nullptr || (reinterpret_cast<uintptr_t>(p->flags[g]) & 7u) != 0) return MOE_EINVAL;
+    if (need_recv) {
+      if (p->recv_x[g] == nullptr || p->recv_meta[g] == nullptr || !aligned16(p->recv_x[g]) ||
+          !aligned16(p->recv_meta[g]))
+        return MOE_EINVAL;
+      if (s.nsc > 0 && (p->recv_scales[g] == nullptr || !aligned4(p->recv_scales[g]))) return MOE_EINVAL;
+    }
+    if (need_y && (p->expert_out[g] == nullptr || !aligned16(p->expert_out[g]))) return MOE_EINVAL;
+    q.recv_x[g] = static_cast<uint8_t *>(p->recv_x[g]);
+    q.recv_scales[g] = p->recv_scales[g];
+    q.recv_meta[g] = reinterpret_cast<int4 *>(p->recv_meta[g]);
+    q.flags[g] = p->flags[g];
+    q.y[g] = static_cast<uint16_t *>(p->expert_out[g]);
+  }
+  *out = q;
+  return MOE_OK;
+}
+
+moe_status launch_layout(const Sizes &s, const int32_t *topk_idx, int32_t *counts, const SlotParts &parts,
                          int32_t *tok_slot, int32_t *err, cudaStream_t stream);
 moe_status launch_dispatch(const Sizes &s, const void *x, const float *x_scales, const int32_t *tok_slot,
-                           const uint64_t *flags, void *recv_x, float *recv_scales, int32_t *recv_meta,
-                           int32_t *err, int num_sms, cudaStream_t stream);
+                           const SlotParts &parts, int32_t *err, int num_sms, cudaStream_t stream);
+moe_status launch_layout_dispatch(const Sizes &s, const int32_t *topk_idx, const void *x, const float *x_scales,
+                                  int32_t *counts, int32_t *tok_slot, const SlotParts &parts, int32_t *err,
+                                  int num_sms, cudaStream_t stream);
+moe_status launch_combine(const Sizes &s, const SlotParts &parts, int64_t y_rows, const float *weights,
+                          const int32_t *tok_slot, uint16_t *out, int32_t *err, cudaStream_t stream);
 
 }  // namespace moe

@@ -30,10 +30,7 @@ struct DispatchArgs {
   const uint8_t *x;
   const float *x_scales;
   const int32_t *tok_slot;
-  const uint64_t *flags;
-  uint8_t *recv_x;
-  float *recv_scales;
-  int4 *recv_meta;
+  SlotParts parts;  // rows, scales, headers and count + 1 flags of the receive side
   int32_t *err;
   int R, T, k, max_m, nsc, stages, pieces, early, quant;
   // row_bytes, piece_bytes: of the caller's input rows. Copy mode dispatches
@@ -105,7 +102,7 @@ __global__ void __launch_bounds__(32) dispatch_kernel(DispatchArgs a) {
         latch_error(a.err, MOE_EINVAL);
         slot = -1;
       } else if (slot >= 0) {
-        if (wait_flag_nonzero(a.flags + slot / a.max_m) == 0) {
+        if (wait_flag_nonzero(flag_ptr(a.parts, slot / a.max_m)) == 0) {
           latch_error(a.err, MOE_ETIMEOUT);
           slot = -1;
         }
@@ -118,14 +115,20 @@ __global__ void __launch_bounds__(32) dispatch_kernel(DispatchArgs a) {
       const int src = static_cast<int>(row / a.T), t = static_cast<int>(row % a.T);
       if (lane < a.k && dst[lane] >= 0) {
         const int32_t slot = dst[lane];
-        a.recv_meta[slot] = make_int4(src, t, (slot / a.max_m) / a.R, lane);
+        int g;
+        const int64_t l = slot_local(a.parts, slot, &g);
+        a.parts.recv_meta[g][l] = make_int4(src, t, (slot / a.max_m) / a.R, lane);
       }
       if (a.nsc > 0 && !a.quant) {
         const float *sc = a.x_scales + row * a.nsc;
         for (int q = lane; q < a.k * a.nsc; q += 32) {
           const int j = q / a.nsc, c = q - j * a.nsc;
           const int32_t slot = dst[j];
-          if (slot >= 0) a.recv_scales[static_cast<int64_t>(slot) * a.nsc + c] = __ldg(sc + c);
+          if (slot >= 0) {
+            int g;
+            const int64_t l = slot_local(a.parts, slot, &g);
+            a.parts.recv_scales[g][l * a.nsc + c] = __ldg(sc + c);
+          }
         }
       }
     }
@@ -152,13 +155,20 @@ __global__ void __launch_bounds__(32) dispatch_kernel(DispatchArgs a) {
       for (int qq = lane; qq < a.k * nblk; qq += 32) {
         const int j = qq / nblk, b = qq - j * nblk;
         const int32_t slot = dst[j];
-        if (slot >= 0) a.recv_scales[static_cast<int64_t>(slot) * a.nsc + sc0 + b] = qs[b];
+        if (slot >= 0) {
+          int g;
+          const int64_t l = slot_local(a.parts, slot, &g);
+          a.parts.recv_scales[g][l * a.nsc + sc0 + b] = qs[b];
+        }
       }
       if (lane == 0) {
         for (int j = 0; j < a.k; ++j) {
           const int32_t slot = dst[j];
-          if (slot >= 0)
-            bulk_store(a.recv_x + static_cast<int64_t>(slot) * (a.row_bytes / 2) + off / 2, q, bytes / 2);
+          if (slot >= 0) {
+            int g;
+            const int64_t l = slot_local(a.parts, slot, &g);
+            bulk_store(a.parts.recv_x[g] + l * (a.row_bytes / 2) + off / 2, q, bytes / 2);
+          }
         }
         bulk_commit();
         // the bf16 stage has been consumed: refill it with unit i + S
@@ -176,7 +186,11 @@ __global__ void __launch_bounds__(32) dispatch_kernel(DispatchArgs a) {
       } else {
         for (int j = 0; j < a.k; ++j) {
           const int32_t slot = dst[j];
-          if (slot >= 0) bulk_store(a.recv_x + static_cast<int64_t>(slot) * a.row_bytes + off, stage, bytes);
+          if (slot >= 0) {
+            int g;
+            const int64_t l = slot_local(a.parts, slot, &g);
+            bulk_store(a.parts.recv_x[g] + l * a.row_bytes + off, stage, bytes);
+          }
         }
         bulk_commit();
         // refill the stage of the previous unit once its stores have read it
@@ -205,16 +219,12 @@ __global__ void __launch_bounds__(32) dispatch_kernel(DispatchArgs a) {
 }
 
 moe_status launch_dispatch(const Sizes &s, const void *x, const float *x_scales, const int32_t *tok_slot,
-                           const uint64_t *flags, void *recv_x, float *recv_scales, int32_t *recv_meta,
-                           int32_t *err, int num_sms, cudaStream_t stream) {
+                           const SlotParts &parts, int32_t *err, int num_sms, cudaStream_t stream) {
   DispatchArgs a{};
   a.x = static_cast<const uint8_t *>(x);
   a.x_scales = x_scales;
   a.tok_slot = tok_slot;
-  a.flags = flags;
-  a.recv_x = static_cast<uint8_t *>(recv_x);
-  a.recv_scales = recv_scales;
-  a.recv_meta = reinterpret_cast<int4 *>(recv_meta);
+  a.parts = parts;
   a.err = err;
   a.R = s.R;
   a.T = s.T;
@@ -277,6 +287,7 @@ extern "C" moe_status moe_dispatch(const moe_desc *desc, const void *x, const fl
   }
   if (!aligned16(x) || !aligned16(recv_x) || !aligned16(recv_meta) || !aligned4(tok_slot) || !aligned4(err))
     return MOE_EINVAL;
-  return launch_dispatch(s, x, x_scales, tok_slot, flags, recv_x, recv_scales, recv_meta, err, desc->num_sms,
-                         static_cast<cudaStream_t>(stream));
+  return launch_dispatch(s, x, x_scales, tok_slot,
+                         single_part(s, recv_x, recv_scales, recv_meta, const_cast<uint64_t *>(flags), nullptr), err,
+                         desc->num_sms, static_cast<cudaStream_t>(stream));
 }

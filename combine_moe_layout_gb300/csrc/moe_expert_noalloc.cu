@@ -8,30 +8,24 @@
 // overlaps in time (different streams, or graphs replayed concurrently) race on
 // it. Rows of the scratch that a call does not write are read only into output
 // rows that are never stored (rows past an expert's end), so it is not cleared.
-#include <mutex>
-
 #include "moe_common.cuh"
 
 namespace {
 
 constexpr size_t kScratchBytes = size_t(32) << 20;  // h of at most R*T*k x I bf16 = 32 MiB
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_expert_h_scratch[kScratchBytes];
 
-// Device address of the scratch on the current device, looked up once per device.
+// Device address of the scratch in the current context. In host code the
+// array's name is only a stand-in, so the address is asked of the runtime on
+// every call: the lookup is a host-side table read once the library's module
+// is loaded in the context, and no address outlives a context (a cached one
+// could, after cudaDeviceReset or with a non-primary context). The first call
+// in a context loads the module: make it before any stream capture.
 void *scratch_address() {
-  static std::mutex mu;
-  static void *addr[kMaxDevices] = {};
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_expert_h_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = p;
-  }
-  return addr[dev];
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_expert_h_scratch) != cudaSuccess) return nullptr;
+  return p;
 }
 
 }  // namespace

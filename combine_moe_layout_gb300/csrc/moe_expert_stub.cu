@@ -14,10 +14,8 @@ constexpr int kStubThreads = 256;
 constexpr int kStubSlotsPerRegionBlock = 8;
 
 struct StubArgs {
-  const uint8_t *q;
-  const float *scales;
+  SlotParts parts;  // the rows and scales read, the expert outputs y written, per part
   const int32_t *counts;
-  uint16_t *y;
   int32_t *err;
   int R, H, max_m, nsc;
 };
@@ -68,11 +66,13 @@ __global__ void __launch_bounds__(kStubThreads) expert_stub_kernel(StubArgs a) {
   }
   const int e = static_cast<int>(region / a.R);
   const double c = 1.0 + static_cast<double>(e) / 256.0;
+  int64_t lr;  // the region within its part
+  const int g = part_split(a.parts.G, a.parts.regions_per_part, region, &lr);
   for (int pos = blockIdx.y; pos < count; pos += gridDim.y) {
-    const int64_t s = region * a.max_m + pos;
-    const uint8_t *q = a.q + s * a.H;
-    const float *sc = a.scales + s * a.nsc;
-    uint16_t *y = a.y + s * a.H;
+    const int64_t s = lr * a.max_m + pos;
+    const uint8_t *q = a.parts.recv_x[g] + s * a.H;
+    const float *sc = a.parts.recv_scales[g] + s * a.nsc;
+    uint16_t *y = a.parts.y[g] + s * a.H;
     for (int h = threadIdx.x * 8; h < a.H; h += kStubThreads * 8) {
       const uint2 packed = *reinterpret_cast<const uint2 *>(q + h);
       const double scale = static_cast<double>(sc[h / kScaleBlock]);
@@ -94,6 +94,15 @@ __global__ void __launch_bounds__(kStubThreads) expert_stub_kernel(StubArgs a) {
 
 using namespace moe;
 
+static moe_status launch_stub(const Sizes &s, const SlotParts &parts, const int32_t *counts, int32_t *err,
+                              cudaStream_t stream) {
+  StubArgs a{parts, counts, err, s.R, s.H, s.max_m, s.nsc};
+  const int per_region = s.max_m < kStubSlotsPerRegionBlock ? s.max_m : kStubSlotsPerRegionBlock;
+  dim3 grid(static_cast<unsigned>(s.E) * s.R, per_region, 1);
+  expert_stub_kernel<<<grid, kStubThreads, 0, stream>>>(a);
+  return launch_status();
+}
+
 extern "C" moe_status moe_expert_stub(const moe_desc *desc, const void *recv_x, const float *recv_scales,
                                       const int32_t *counts, uint16_t *expert_out, int32_t *err, void *stream) {
   Sizes s;
@@ -104,9 +113,20 @@ extern "C" moe_status moe_expert_stub(const moe_desc *desc, const void *recv_x, 
     return MOE_EINVAL;
   if (!aligned16(recv_x) || !aligned16(expert_out) || !aligned4(recv_scales) || !aligned4(counts))
     return MOE_EINVAL;
-  StubArgs a{static_cast<const uint8_t *>(recv_x), recv_scales, counts, expert_out, err, s.R, s.H, s.max_m, s.nsc};
-  const int per_region = s.max_m < kStubSlotsPerRegionBlock ? s.max_m : kStubSlotsPerRegionBlock;
-  dim3 grid(static_cast<unsigned>(s.E) * s.R, per_region, 1);
-  expert_stub_kernel<<<grid, kStubThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
-  return launch_status();
+  SlotParts p = single_part(s, const_cast<void *>(recv_x), const_cast<float *>(recv_scales), nullptr, nullptr,
+                            expert_out);
+  return launch_stub(s, p, counts, err, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" moe_status moe_expert_stub_parts(const moe_desc *desc, const moe_parts *parts, const int32_t *counts,
+                                            int32_t *err, void *stream) {
+  Sizes s;
+  moe_status st = check_desc(desc, &s);
+  if (st != MOE_OK) return st;
+  if (s.dtype == MOE_BF16) return MOE_EINVAL;
+  SlotParts p;
+  st = parts_from(s, parts, true, true, &p);
+  if (st != MOE_OK) return st;
+  if (counts == nullptr || err == nullptr || !aligned4(counts)) return MOE_EINVAL;
+  return launch_stub(s, p, counts, err, static_cast<cudaStream_t>(stream));
 }

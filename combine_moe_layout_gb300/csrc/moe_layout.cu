@@ -46,7 +46,7 @@ constexpr int kLayoutMaxExperts = 8192;
 struct LayoutArgs {
   const int32_t *topk_idx;
   int32_t *counts;
-  uint64_t *flags;
+  SlotParts parts;  // only the flags are written
   int32_t *tok_slot;
   int32_t *err;
   int R, T, E, k, max_m, early;
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(LayoutArgs a) {
       for (int w = 0; w < kLayoutWords; ++w) c += __popc(bits[e * kLayoutWords + w]);
       const int64_t r = static_cast<int64_t>(e) * a.R + src;
       a.counts[r] = c;
-      a.flags[r] = static_cast<uint64_t>(c) + 1;
+      *flag_ptr(a.parts, r) = static_cast<uint64_t>(c) + 1;
     }
   }
 }
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kClusterThreads) layout_cluster_kernel(LayoutA
       const int c = b + hist[e];
       const int64_t reg = static_cast<int64_t>(e) * a.R + src;
       a.counts[reg] = c;
-      a.flags[reg] = static_cast<uint64_t>(c) + 1;
+      *flag_ptr(a.parts, reg) = static_cast<uint64_t>(c) + 1;
     }
   }
   __syncthreads();
@@ -232,10 +232,10 @@ int sm_count() {
   return n;
 }
 
-moe_status launch_layout(const Sizes &s, const int32_t *topk_idx, int32_t *counts, uint64_t *flags,
+moe_status launch_layout(const Sizes &s, const int32_t *topk_idx, int32_t *counts, const SlotParts &parts,
                          int32_t *tok_slot, int32_t *err, cudaStream_t stream) {
   if (s.E > kLayoutMaxExperts) return MOE_EINVAL;
-  LayoutArgs a{topk_idx, counts, flags, tok_slot, err, s.R, s.T, s.E, s.k, s.max_m, early_trigger(s.ntok)};
+  LayoutArgs a{topk_idx, counts, parts, tok_slot, err, s.R, s.T, s.E, s.k, s.max_m, early_trigger(s.ntok)};
   int csize = 0, tpc = 0, words = 0;
   size_t csmem = 0;
   if (cluster_shape(s, &csize, &tpc, &words, &csmem)) {
@@ -306,7 +306,8 @@ extern "C" moe_status moe_layout(const moe_desc *desc, const int32_t *topk_idx, 
   if (!aligned4(topk_idx) || !aligned4(counts) || !aligned4(tok_slot) || !aligned4(err) ||
       (reinterpret_cast<uintptr_t>(flags) & 7u) != 0)
     return MOE_EINVAL;
-  return launch_layout(s, topk_idx, counts, flags, tok_slot, err, static_cast<cudaStream_t>(stream));
+  return launch_layout(s, topk_idx, counts, single_part(s, nullptr, nullptr, nullptr, flags, nullptr), tok_slot, err,
+                       static_cast<cudaStream_t>(stream));
 }
 
 extern "C" moe_status moe_reset(const moe_desc *desc, uint64_t *flags, int32_t *err, void *stream) {
@@ -317,6 +318,22 @@ extern "C" moe_status moe_reset(const moe_desc *desc, uint64_t *flags, int32_t *
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(flags, 0, static_cast<size_t>(s.E) * s.R * sizeof(uint64_t), cs) != cudaSuccess)
     return MOE_ECUDA;
+  if (cudaMemsetAsync(err, 0, sizeof(int32_t), cs) != cudaSuccess) return MOE_ECUDA;
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_reset_parts(const moe_desc *desc, const moe_parts *parts, int32_t *err, void *stream) {
+  Sizes s;
+  moe_status st = check_desc(desc, &s);
+  if (st != MOE_OK) return st;
+  SlotParts p;
+  st = parts_from(s, parts, false, false, &p);
+  if (st != MOE_OK) return st;
+  if (err == nullptr) return MOE_EINVAL;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  for (int g = 0; g < p.G; ++g)
+    if (cudaMemsetAsync(p.flags[g], 0, static_cast<size_t>(p.regions_per_part) * sizeof(uint64_t), cs) != cudaSuccess)
+      return MOE_ECUDA;
   if (cudaMemsetAsync(err, 0, sizeof(int32_t), cs) != cudaSuccess) return MOE_ECUDA;
   return MOE_OK;
 }

@@ -43,19 +43,16 @@ constexpr int kFusedHistRows = 32;       // rows per rank that also count expert
 struct FusedArgs {
   const int32_t *topk_idx;
   int32_t *counts;
-  uint64_t *flags;
   int32_t *tok_slot;
   const uint8_t *x;
   const float *x_scales;
-  uint8_t *recv_x;
-  float *recv_scales;
-  int4 *recv_meta;
+  SlotParts parts;  // rows, scales, headers and count + 1 flags of the receive side
   int32_t *err;
   int R, T, E, k, max_m, nsc, G, early;
   int vin;      // W-byte vectors of a caller's input row
   int idx_vec;  // a rank's routing can be read as int4 (T*k % 4 == 0, 16-byte aligned base)
   int sc_vec;   // scales move as float4 (nsc % 4 == 0, both scale arrays 16-byte aligned)
-  uint32_t row_bytes;     // a dispatched row: the slot stride of recv_x
+  uint32_t row_bytes;     // a dispatched row: the slot stride of the receive rows
   uint32_t in_row_bytes;  // a caller's input row
   int64_t nrows;
 };
@@ -114,6 +111,8 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
   __shared__ int32_t s_part[kFusedWarps][KC];
   __shared__ int32_t s_own[KC];
   __shared__ int32_t s_slot[KC];
+  __shared__ uint8_t *s_dst[KC];  // each choice's slot row (in its part)
+  __shared__ float *s_dsc[KC];    // and its scales
   extern __shared__ int32_t s_hist[];  // [G]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -238,6 +237,12 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
       }
       my_e = e;
       s_slot[tid] = my_slot;
+      if (my_slot >= 0) {
+        int g;
+        const int64_t l = slot_local(a.parts, my_slot, &g);
+        s_dst[tid] = a.parts.recv_x[g] + l * a.row_bytes;
+        s_dsc[tid] = a.nsc > 0 ? a.parts.recv_scales[g] + l * a.nsc : nullptr;
+      }
     }
     __syncthreads();
 
@@ -247,16 +252,15 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
 #pragma unroll
       for (int j = 0; j < KC; ++j) {
         if (j >= a.k) break;
-        const int32_t slot = s_slot[j];
-        if (slot < 0) continue;
-        uint8_t *dst = a.recv_x + static_cast<int64_t>(slot) * a.row_bytes;
+        if (s_slot[j] < 0) continue;
+        uint8_t *dst = s_dst[j];
 #pragma unroll
         for (int u = 0; u < VPT; ++u) {
           const int q = tid + u * kFusedThreads;
           if (q < a.vin) st_row<W>(dst + static_cast<int64_t>(q) * W, v[u], pol);
         }
         if (a.nsc > 0) {
-          float *ds = a.recv_scales + static_cast<int64_t>(slot) * a.nsc;
+          float *ds = s_dsc[j];
           if (a.sc_vec) {
             if (tid < a.nsc / 4) reinterpret_cast<float4 *>(ds)[tid] = sc;
           } else if (tid < a.nsc) {
@@ -310,11 +314,10 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
 #pragma unroll
         for (int j = 0; j < KC; ++j) {
           if (j >= a.k) break;
-          const int32_t slot = s_slot[j];
-          if (slot < 0) continue;
-          uint8_t *dst = a.recv_x + static_cast<int64_t>(slot) * a.row_bytes;
+          if (s_slot[j] < 0) continue;
+          uint8_t *dst = s_dst[j];
           if (store16) st_row<16>(dst + static_cast<int64_t>(q) * NE, out16, pol);
-          if (q % G == 0) a.recv_scales[static_cast<int64_t>(slot) * a.nsc + q / G] = s;
+          if (q % G == 0) s_dsc[j][q / G] = s;
         }
       }
     }
@@ -324,13 +327,17 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
     //    this row's share of the experts
     if (tid < a.k) {
       a.tok_slot[row * a.k + tid] = my_slot;
-      if (my_slot >= 0) a.recv_meta[my_slot] = make_int4(src, t, my_e, tid);
+      if (my_slot >= 0) {
+        int g;
+        const int64_t l = slot_local(a.parts, my_slot, &g);
+        a.parts.recv_meta[g][l] = make_int4(src, t, my_e, tid);
+      }
     }
     for (int i = tid; i < hn; i += kFusedThreads) {
       const int c = s_hist[i];
       const int64_t r = static_cast<int64_t>(h0 + i) * a.R + src;
       a.counts[r] = c;
-      a.flags[r] = static_cast<uint64_t>(c) + 1;
+      *flag_ptr(a.parts, r) = static_cast<uint64_t>(c) + 1;
     }
     if (row + gridDim.x < a.nrows) __syncthreads();  // the next row reuses the shared arrays
   }
@@ -406,32 +413,33 @@ static moe_status launch_fused_w(const FusedArgs &a, int width, int sms, cudaStr
 }
 
 moe_status launch_layout_dispatch(const Sizes &s, const int32_t *topk_idx, const void *x, const float *x_scales,
-                                  int32_t *counts, uint64_t *flags, int32_t *tok_slot, void *recv_x,
-                                  float *recv_scales, int32_t *recv_meta, int32_t *err, int num_sms,
-                                  cudaStream_t stream) {
+                                  int32_t *counts, int32_t *tok_slot, const SlotParts &parts, int32_t *err,
+                                  int num_sms, cudaStream_t stream) {
   if (!fused_fits(s)) {
-    moe_status st = launch_layout(s, topk_idx, counts, flags, tok_slot, err, stream);
+    moe_status st = launch_layout(s, topk_idx, counts, parts, tok_slot, err, stream);
     if (st != MOE_OK || s.ntok == 0) return st;
-    return launch_dispatch(s, x, x_scales, tok_slot, flags, recv_x, recv_scales, recv_meta, err, num_sms, stream);
+    return launch_dispatch(s, x, x_scales, tok_slot, parts, err, num_sms, stream);
   }
   // Vector width, measured on GB300: plain copies of rows up to 8 KiB are
   // fastest with 16-byte vectors (ds_decode step 36.6 vs 37.6 us with 32-byte
   // ones), longer rows and quantised rows with 32-byte vectors (skewed 162.3
   // vs 163.4 us; ds_decode with bf16 rows 46.1 vs 56.6 us), where the rows and
   // pointers allow them.
-  const bool can32 = s.in_row_bytes % 32 == 0 && aligned32(x) &&
-                     (s.quant || (s.row_bytes % 32 == 0 && aligned32(recv_x)));
+  bool rows32 = s.row_bytes % 32 == 0;
+  bool scales16 = true;
+  for (int g = 0; g < parts.G; ++g) {
+    rows32 = rows32 && aligned32(parts.recv_x[g]);
+    scales16 = scales16 && aligned16(parts.recv_scales[g]);
+  }
+  const bool can32 = s.in_row_bytes % 32 == 0 && aligned32(x) && (s.quant || rows32);
   const bool wide = can32 && (s.quant || s.in_row_bytes > kFusedNarrowMaxRow);
   FusedArgs a{};
   a.topk_idx = topk_idx;
   a.counts = counts;
-  a.flags = flags;
   a.tok_slot = tok_slot;
   a.x = static_cast<const uint8_t *>(x);
   a.x_scales = x_scales;
-  a.recv_x = static_cast<uint8_t *>(recv_x);
-  a.recv_scales = recv_scales;
-  a.recv_meta = reinterpret_cast<int4 *>(recv_meta);
+  a.parts = parts;
   a.err = err;
   a.R = s.R;
   a.T = s.T;
@@ -443,7 +451,7 @@ moe_status launch_layout_dispatch(const Sizes &s, const int32_t *topk_idx, const
   a.early = early_trigger(s.ntok);
   a.vin = static_cast<int>(s.in_row_bytes / (wide ? 32 : 16));
   a.idx_vec = (static_cast<int64_t>(s.T) * s.k) % 4 == 0 && aligned16(topk_idx) ? 1 : 0;
-  a.sc_vec = s.nsc % 4 == 0 && aligned16(x_scales) && aligned16(recv_scales) ? 1 : 0;
+  a.sc_vec = s.nsc % 4 == 0 && aligned16(x_scales) && scales16 ? 1 : 0;
   a.row_bytes = static_cast<uint32_t>(s.row_bytes);
   a.in_row_bytes = static_cast<uint32_t>(s.in_row_bytes);
   a.nrows = s.ntok;
@@ -478,8 +486,29 @@ extern "C" moe_status moe_layout_dispatch(const moe_desc *desc, const int32_t *t
   if (!aligned16(x) || !aligned16(recv_x) || !aligned16(recv_meta) || !aligned4(tok_slot) || !aligned4(err) ||
       !aligned4(topk_idx) || !aligned4(counts) || (reinterpret_cast<uintptr_t>(flags) & 7u) != 0)
     return MOE_EINVAL;
-  return launch_layout_dispatch(s, topk_idx, x, x_scales, counts, flags, tok_slot, recv_x, recv_scales, recv_meta,
-                                err, desc->num_sms, static_cast<cudaStream_t>(stream));
+  return launch_layout_dispatch(s, topk_idx, x, x_scales, counts, tok_slot,
+                                single_part(s, recv_x, recv_scales, recv_meta, flags, nullptr), err, desc->num_sms,
+                                static_cast<cudaStream_t>(stream));
+}
+
+extern "C" moe_status moe_layout_dispatch_parts(const moe_desc *desc, const int32_t *topk_idx, const void *x,
+                                                const float *x_scales, int32_t *counts, int32_t *tok_slot,
+                                                const moe_parts *parts, int32_t *err, void *stream) {
+  Sizes s;
+  moe_status st = check_desc(desc, &s);
+  if (st != MOE_OK) return st;
+  SlotParts p;
+  st = parts_from(s, parts, true, false, &p);
+  if (st != MOE_OK) return st;
+  if (counts == nullptr || err == nullptr) return MOE_EINVAL;
+  if (s.ntok > 0 && (topk_idx == nullptr || tok_slot == nullptr || x == nullptr)) return MOE_EINVAL;
+  if (s.dtype == MOE_FP8_E4M3 && (s.ntok > 0 && x_scales == nullptr)) return MOE_EINVAL;
+  if (s.dtype != MOE_FP8_E4M3 && x_scales != nullptr) return MOE_EINVAL;
+  if (!aligned16(x) || !aligned4(x_scales) || !aligned4(tok_slot) || !aligned4(err) || !aligned4(topk_idx) ||
+      !aligned4(counts))
+    return MOE_EINVAL;
+  return launch_layout_dispatch(s, topk_idx, x, x_scales, counts, tok_slot, p, err, desc->num_sms,
+                                static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int32_t moe_layout_dispatch_kernels(const moe_desc *desc) {

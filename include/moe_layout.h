@@ -295,9 +295,11 @@ moe_status moe_expert_down_fp8(const moe_desc *desc, int32_t inter, const int32_
  * callers that may not allocate device memory. h is kept in a fixed device array
  * of the library (32 MiB), so R*T*k * inter * 2 bytes may not exceed 32 MiB
  * (MOE_ENOMEM otherwise, nothing launched). The array is shared by all calls on
- * a device: calls whose work overlaps in time race on it. Arguments, results
- * and other errors as moe_expert_gate_up and moe_expert_down; MOE_ECUDA if the
- * array's address cannot be obtained. */
+ * a device: calls whose work overlaps in time race on it. Its address is asked
+ * of the CUDA runtime on every call (valid in whatever context is current); the
+ * first call in a context loads the library's module, so make it before any
+ * stream capture. Arguments, results and other errors as moe_expert_gate_up
+ * and moe_expert_down; MOE_ECUDA if the array's address cannot be obtained. */
 moe_status moe_expert_mlp_noalloc(const moe_desc *desc, int32_t inter, const int32_t *region_offsets,
                                   const void *packed_x, const void *w_gate, const void *w_up, const void *w_down,
                                   void *packed_y, int32_t *err, void *stream);
@@ -331,6 +333,52 @@ moe_status moe_combine(const moe_desc *desc, const uint16_t *expert_out, const f
 /* Clear flags [E][R] and the error word (for the first step, or after an
  * aborted one). */
 moe_status moe_reset(const moe_desc *desc, uint64_t *flags, int32_t *err, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Partitioned slot buffers: the receive side split the way the GPUs of an EP
+ * group hold it (Perplexity, "NVSHMEM": each rank owns its private receive
+ * buffers and a sender puts its rows there, then signals; "Combine": the
+ * receiver's results are read back per token). With G parts (G divides R,
+ * 1 <= G <= MOE_MAX_PARTS), part g holds the regions of ranks
+ * [g*R/G, (g+1)*R/G): its recv_x, recv_scales, recv_meta and expert_out hold
+ * global slots [g*P, (g+1)*P) at local slot s - g*P, with P = E*R*max_m / G,
+ * and its flags hold regions [g*E*R/G, (g+1)*E*R/G) likewise; each buffer is
+ * 1/G of the size moe_buffer_sizes gives. Slot ids (tok_slot, the slot
+ * headers) and counts [E][R] stay global. The parts may be separate
+ * allocations; every part is written with plain stores only.
+ * --------------------------------------------------------------------------- */
+#define MOE_MAX_PARTS 8
+
+typedef struct {
+  int32_t num_parts;                     /* G */
+  void *recv_x[MOE_MAX_PARTS];           /* 16-byte aligned */
+  float *recv_scales[MOE_MAX_PARTS];     /* NULL for bf16 rows; 4-byte aligned */
+  int32_t *recv_meta[MOE_MAX_PARTS];     /* 16-byte aligned */
+  uint64_t *flags[MOE_MAX_PARTS];        /* 8-byte aligned */
+  void *expert_out[MOE_MAX_PARTS];       /* bf16 rows of H, 16-byte aligned; NULL where not used */
+} moe_parts;
+
+/* moe_layout_dispatch with the receive side in parts (see above): the same
+ * results, each slot's row, scales and header in its part, each count + 1 flag
+ * in its part; counts and tok_slot global. Reads nothing before its dependency
+ * wait. Errors as moe_layout_dispatch; an invalid part table -> MOE_EINVAL. */
+moe_status moe_layout_dispatch_parts(const moe_desc *desc, const int32_t *topk_idx, const void *x,
+                                     const float *x_scales, int32_t *counts, int32_t *tok_slot,
+                                     const moe_parts *parts, int32_t *err, void *stream);
+
+/* moe_combine reading each expert output row from its part (parts->expert_out;
+ * for bf16 identity experts the caller may pass the recv_x parts there) and
+ * clearing every part's flags. */
+moe_status moe_combine_parts(const moe_desc *desc, const moe_parts *parts, const float *topk_weights,
+                             const int32_t *tok_slot, uint16_t *out, int32_t *err, void *stream);
+
+/* moe_expert_stub over parts: reads each part's rows and scales, writes its
+ * expert_out rows. Test and benchmark support, like moe_expert_stub. */
+moe_status moe_expert_stub_parts(const moe_desc *desc, const moe_parts *parts, const int32_t *counts, int32_t *err,
+                                 void *stream);
+
+/* moe_reset over parts: clears every part's flags and the error word. */
+moe_status moe_reset_parts(const moe_desc *desc, const moe_parts *parts, int32_t *err, void *stream);
 
 /* Synchronise `stream`, read the device error word, clear it, and return its
  * value (MOE_OK if no kernel latched an error). Host-synchronising. */
