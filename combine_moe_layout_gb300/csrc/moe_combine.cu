@@ -39,8 +39,11 @@ struct CombineArgs {
   int64_t nslots;  // rows of y: the slots (fixed-slot layout) or the packed rows
 };
 
-// Row `slot` of y, in its part.
+// Row `slot` of y, in its part (PARTS: more than one part; one part is the
+// single buffer, with the address arithmetic of a plain array).
+template <bool PARTS>
 __device__ __forceinline__ const uint16_t *y_row(const CombineArgs &a, int32_t slot) {
+  if constexpr (!PARTS) return a.parts.y[0] + static_cast<int64_t>(slot) * a.H;
   int g;
   const int64_t l = slot_local(a.parts, slot, &g);
   return a.parts.y[g] + l * a.H;
@@ -88,7 +91,7 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
 // 668 us per combine inside the step), slower for decode-sized batches.
 constexpr int64_t kCombineTmaMinTokens = 16384;
 
-template <int K>
+template <int K, bool PARTS>
 __global__ void __launch_bounds__(kCombineThreads) combine_tma_kernel(CombineArgs a) {
   __shared__ __align__(128) uint4 stage[K][kCombineThreads];
   __shared__ uint64_t bar;
@@ -126,7 +129,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_tma_kernel(CombineArg
     mbar_arrive_expect_tx(&bar, nvalid * bytes);
     for (int j = 0; j < K; ++j)
       if (s_slot[j] >= 0)
-        bulk_load(&stage[j][0], y_row(a, s_slot[j]) + static_cast<int64_t>(v0) * 8, bytes,
+        bulk_load(&stage[j][0], y_row<PARTS>(a, s_slot[j]) + static_cast<int64_t>(v0) * 8, bytes,
                   &bar);
   }
   if (!mbar_wait_bounded(&bar, 0)) {
@@ -149,7 +152,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_tma_kernel(CombineArg
 // Block b handles token b / chunks, column vectors [c*128*VPT, (c+1)*128*VPT)
 // with c = b % chunks; each thread owns VPT vectors and issues all their k
 // loads before it computes.
-template <int K, int VPT>
+template <int K, int VPT, bool PARTS>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a) {
   constexpr int KC = K > 0 ? K : kMaxTopk;
   const int k = K > 0 ? K : a.k;
@@ -186,7 +189,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
     for (int j = 0; j < KC; ++j)
       if (j < k)
         y[u][j] = (v < V && slot[j] >= 0)
-                      ? __ldcs(reinterpret_cast<const uint4 *>(y_row(a, slot[j])) + v)
+                      ? __ldcs(reinterpret_cast<const uint4 *>(y_row<PARTS>(a, slot[j])) + v)
                       : make_uint4(0, 0, 0, 0);
   }
   uint4 *dst = reinterpret_cast<uint4 *>(a.out + tok * a.H);
@@ -219,13 +222,18 @@ moe_status launch_combine_k(CombineArgs a, int64_t ntok, cudaStream_t stream) {
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   use_pdl(cfg, attr);
+  const bool parts = a.parts.G > 1;
   if constexpr (K >= 4) {
     if (tma) {
-      if (cudaLaunchKernelEx(&cfg, combine_tma_kernel<K>, a) != cudaSuccess) return MOE_ECUDA;
+      if (cudaLaunchKernelEx(&cfg, parts ? combine_tma_kernel<K, true> : combine_tma_kernel<K, false>, a) !=
+          cudaSuccess)
+        return MOE_ECUDA;
       return launch_status();
     }
   }
-  if (cudaLaunchKernelEx(&cfg, combine_kernel<K, VPT>, a) != cudaSuccess) return MOE_ECUDA;
+  if (cudaLaunchKernelEx(&cfg, parts ? combine_kernel<K, VPT, true> : combine_kernel<K, VPT, false>, a) !=
+      cudaSuccess)
+    return MOE_ECUDA;
   return launch_status();
 }
 
