@@ -1031,14 +1031,22 @@ def run_reference(args, rank, local_rank, world):
 
 
 def calibrate(local_rank: int) -> dict:
-    """Bandwidth of torch's fill (write only) and copy (read + write) kernels over
-    a range of sizes around the step's, timed like the step (L2 flushed before each)."""
+    """Bandwidth of plain device writes (torch's float32 fill: 16-byte stores), reads
+    (a float32 matrix-vector product, which reads its matrix once) and copies (read + write) over a range of sizes around the
+    step's, each timed like the step (L2 flushed before each, CUDA events, median
+    of 100), the time of an empty launch, and a floor for the decode step built
+    from these rates: a launch, then dispatch's bytes at the write and read rates,
+    then combine's at the read and write rates."""
     import torch
+
+    from combine_moe_layout_gb300 import workloads as wl
+
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_w = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     flush_r = torch.ones(flush_w.numel() // 4, dtype=torch.float32, device=dev)
+    tiny = torch.empty(4, dtype=torch.float32, device=dev)
 
     def timeit(fn, n=100):
         for _ in range(5):
@@ -1055,15 +1063,35 @@ def calibrate(local_rank: int) -> dict:
         torch.cuda.synchronize()
         return statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
 
+    launch_us = timeit(lambda: tiny.fill_(1.0))
     rows = []
     for mb in (15, 30, 60, 120, 240, 480, 960):
-        a = torch.empty(mb << 20, dtype=torch.uint8, device=dev)
+        n = mb << 20
+        a = torch.empty(n // 4, dtype=torch.float32, device=dev)
         b = torch.empty_like(a)
-        fill_us = timeit(lambda: a.fill_(7))
+        a.fill_(1.0)
+        mat = a.view(-1, 4096)
+        vec = torch.ones(4096, dtype=torch.float32, device=dev)
+        fill_us = timeit(lambda: a.fill_(7.0))
+        read_us = timeit(lambda: torch.mv(mat, vec))  # reads the matrix once (cuBLAS GEMV)
         copy_us = timeit(lambda: b.copy_(a))
-        rows.append({"MiB": mb, "fill_us": round(fill_us, 2), "fill_GBps": round((mb << 20) / fill_us / 1e3, 1),
-                     "copy_us": round(copy_us, 2), "copy_GBps_read_plus_write": round(2 * (mb << 20) / copy_us / 1e3, 1)})
+        rows.append({"MiB": mb, "fill_us": round(fill_us, 2), "fill_GBps": round(n / fill_us / 1e3, 1),
+                     "read_us": round(read_us, 2), "read_GBps": round(n / read_us / 1e3, 1),
+                     "copy_us": round(copy_us, 2), "copy_GBps_read_plus_write": round(2 * n / copy_us / 1e3, 1)})
         del a, b
+
+    def rate(kind, mib):  # GB/s of the launch-free part, at the nearest measured size
+        r = min(rows, key=lambda r_: abs(r_["MiB"] - mib))
+        return (r["MiB"] << 20) / max(r[kind + "_us"] - launch_us, 1e-3) / 1e3
+
+    w = wl.WORKLOADS["ds_decode"]
+    N, k, H, sc = w.num_tokens, w.topk, w.hidden, w.scales_per_row * 4
+    disp_w = N * k * (w.row_bytes + sc + 16) + N * k * 4
+    disp_r = N * (w.in_row_bytes + sc)
+    comb_r = N * k * 2 * H + N * k * 8
+    comb_w = N * 2 * H
+    wr, rd = rate("fill", disp_w / 2**20), rate("read", comb_r / 2**20)
+    floor_us = launch_us + (disp_w / wr + disp_r / rd + comb_r / rd + comb_w / wr) / 1e3
     host = []
     for mb in (7.5, 15, 60, 240):
         n = int(mb * (1 << 20))
@@ -1074,9 +1102,18 @@ def calibrate(local_rank: int) -> dict:
         host.append({"MiB": mb, "h2d_us": round(h2d_us, 2), "h2d_GBps": round(n / h2d_us / 1e3, 1),
                      "d2h_us": round(d2h_us, 2), "d2h_GBps": round(n / d2h_us / 1e3, 1)})
         del h, dd
-    return {"calibration": "torch fill (write only) and copy (read + write), L2 flushed before each, median of 100; "
-                           "pinned host <-> device copies, median of 50",
-            "gpu": torch.cuda.get_device_name(dev), "rows": rows, "host_copies": host}
+    return {"calibration": "torch float32 fill (16-byte stores: write only), a float32 matrix-vector product "
+                           "(cuBLAS GEMV: reads the matrix once) and copy (read + write), L2 flushed before each, "
+                           "median of 100; pinned host <-> device copies, median of 50",
+            "gpu": torch.cuda.get_device_name(dev), "empty_launch_us": round(launch_us, 2), "rows": rows,
+            "host_copies": host,
+            "ds_decode_floor": {"us": round(floor_us, 2), "write_GBps": round(wr, 1), "read_GBps": round(rd, 1),
+                                "bytes": {"dispatch_write": disp_w, "dispatch_read": disp_r,
+                                          "combine_read": comb_r, "combine_write": comb_w},
+                                "model": "one launch + dispatch writes and combine's output at the plain-write "
+                                         "rate + dispatch and combine reads at the plain-read rate, each rate "
+                                         "taken without its launch time at the nearest measured size; layout "
+                                         "latency and the second kernel's launch are not counted"}}
 
 
 def main(argv=None):
