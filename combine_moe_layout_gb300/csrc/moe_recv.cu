@@ -9,18 +9,19 @@
 // is a separate hook the caller runs when it wants the data, after a send that
 // only issued its writes.
 //
-// Two kernels, chained by programmatic dependent launch:
-//   region_scan_kernel  one CTA: a bounded wait on each region's flag, a check
-//                       that flag - 1 == count <= max_m, and the exclusive scan
-//                       of the counts in (expert, source rank) order.
-//   compact_kernel      one warp per packed row p < R*T*k: binary search of the
-//                       region holding p, then the row, its scales and its
-//                       header copied with 16-byte loads and stores, and p
-//                       recorded in tok_packed[src][t][j] (the forward map the
-//                       packed combine gathers through; -1 for a choice with
-//                       no slot, which that warp's index p also covers). The grid is
-//                       the largest possible packed size, so the host needs no
-//                       count and the call stays asynchronous.
+// One kernel, recv_kernel, for up to kRecvMaxRegions (expert, source) regions:
+// every CTA computes the exclusive scan of the counts (clamped to max_m) in
+// its shared memory, the CTAs share the bounded waits on the regions' flags
+// (and the check flag - 1 == count <= max_m), CTA 0 writes region_offsets, and
+// then one warp per packed row p < R*T*k finds p's region by binary search in
+// shared memory and copies the row, its scales and its header with 16-byte
+// loads and stores, recording p in tok_packed[src][t][j] (the forward map the
+// packed combine gathers through; -1 for a choice with no slot, which that
+// warp's index p also covers). The grid is the resident capacity and the rows
+// are the largest possible packed size, so the host needs no count and the
+// call stays asynchronous. With more regions, two kernels chained by
+// programmatic dependent launch do the same: region_scan_kernel (one CTA: the
+// waits, the checks, the scan) and compact_kernel (the rows).
 #include "moe_common.cuh"
 
 namespace moe {
@@ -104,6 +105,8 @@ struct CompactArgs {
   uint32_t row_bytes;
 };
 
+__device__ __forceinline__ void copy_packed_row(const CompactArgs &a, int64_t p, int64_t slot, int lane);
+
 __global__ void __launch_bounds__(kCompactWarps * 32) compact_kernel(CompactArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t p = static_cast<int64_t>(blockIdx.x) * kCompactWarps + (threadIdx.x >> 5);
@@ -125,11 +128,27 @@ __global__ void __launch_bounds__(kCompactWarps * 32) compact_kernel(CompactArgs
   const int64_t pos = p - a.region_offsets[lo];
   if (pos < 0 || pos >= a.max_m) return;
   const int64_t slot = lo * a.max_m + pos;
+  copy_packed_row(a, p, slot, lane);
+}
+
+constexpr int kRecvThreads = 256;
+constexpr int kRecvWarps = kRecvThreads / 32;
+constexpr int64_t kRecvMaxRegions = 8192;
+
+struct RecvArgs {
+  const int32_t *counts;
+  const uint64_t *flags;
+  int32_t *region_offsets;
+  int32_t *err;
+  CompactArgs c;
+  int early;
+};
+
+// One pass of the 16-byte row copy of packed row p from slot `slot`, shared by
+// both forms of the receive hook.
+__device__ __forceinline__ void copy_packed_row(const CompactArgs &a, int64_t p, int64_t slot, int lane) {
   const uint4 *src = reinterpret_cast<const uint4 *>(a.recv_x + slot * a.row_bytes);
   uint4 *dst = reinterpret_cast<uint4 *>(a.packed_x + p * a.row_bytes);
-  // kCopyBatch loads in flight per lane before their stores: one dependent
-  // load -> store per 16 bytes would leave a warp with 512 bytes in flight,
-  // too little to cover DRAM latency with the warps an SM holds
   const uint32_t nv = a.row_bytes / 16;
   uint32_t v = lane;
   for (; v + (kCopyBatch - 1) * 32 < nv; v += kCopyBatch * 32) {
@@ -145,8 +164,74 @@ __global__ void __launch_bounds__(kCompactWarps * 32) compact_kernel(CompactArgs
     // the header {src, t, e, j} also gives combine its forward map to the packed row
     const int4 m = a.recv_meta[slot];
     a.packed_meta[p] = m;
-    if (m.y >= 0 && m.y < a.T && m.w >= 0 && m.w < a.k && m.x >= 0 && static_cast<int64_t>(m.x) * a.T * a.k < a.npacked_max)
+    if (m.y >= 0 && m.y < a.T && m.w >= 0 && m.w < a.k && m.x >= 0 &&
+        static_cast<int64_t>(m.x) * a.T * a.k < a.npacked_max)
       a.tok_packed[(static_cast<int64_t>(m.x) * a.T + m.y) * a.k + m.w] = static_cast<int32_t>(p);
+  }
+}
+
+__global__ void __launch_bounds__(kRecvThreads) recv_kernel(RecvArgs a) {
+  extern __shared__ int32_t s_off[];  // [nreg + 1]: exclusive scan of the clamped counts, then the total
+  __shared__ int32_t warp_sums[kRecvWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nreg = static_cast<int>(a.c.nreg);
+  grid_dependency_wait();
+  if (a.early) grid_dependents_launch();
+
+  // this CTA's share of the regions: bounded wait on the count + 1 flag, checks
+  for (int r = blockIdx.x * kRecvThreads + tid; r < nreg; r += gridDim.x * kRecvThreads) {
+    const int c = a.counts[r];
+    const uint64_t f = wait_flag_nonzero(a.flags + r);
+    if (f == 0)
+      latch_error(a.err, MOE_ETIMEOUT);
+    else if (f - 1 != static_cast<uint64_t>(c))
+      latch_error(a.err, MOE_EINVAL);  // counts and flags of different steps
+    if (c < 0 || c > a.c.max_m) latch_error(a.err, MOE_EOVERFLOW);
+  }
+
+  // exclusive scan of the clamped counts: thread tid owns regions [r0, r1)
+  const int per = (nreg + kRecvThreads - 1) / kRecvThreads;
+  const int r0 = min(tid * per, nreg), r1 = min(r0 + per, nreg);
+  int sum = 0;
+  for (int r = r0; r < r1; ++r) sum += min(max(a.counts[r], 0), a.c.max_m);
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += warp_sums[w];
+  int acc = before + incl - sum;
+  for (int r = r0; r < r1; ++r) {
+    s_off[r] = acc;
+    acc += min(max(a.counts[r], 0), a.c.max_m);
+  }
+  if (tid == kRecvThreads - 1) s_off[nreg] = acc;
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int r = tid; r <= nreg; r += kRecvThreads) a.region_offsets[r] = s_off[r];
+  const int64_t total = s_off[nreg];
+
+  // the rows: one warp per packed row
+  for (int64_t p = static_cast<int64_t>(blockIdx.x) * kRecvWarps + warp; p < a.c.npacked_max;
+       p += static_cast<int64_t>(gridDim.x) * kRecvWarps) {
+    // choice p with no slot (masked, or rejected by layout) has no packed row
+    if (lane == 0 && a.c.tok_slot[p] < 0) a.c.tok_packed[p] = -1;
+    if (p >= total) continue;
+    int lo = 0, hi = nreg - 1;  // the region with s_off[lo] <= p < s_off[lo + 1]
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) / 2;
+      if (s_off[mid] <= p)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int64_t pos = p - s_off[lo];
+    if (pos < 0 || pos >= a.c.max_m) continue;
+    copy_packed_row(a.c, p, static_cast<int64_t>(lo) * a.c.max_m + pos, lane);
   }
 }
 
@@ -154,7 +239,37 @@ moe_status launch_recv(const Sizes &s, const int32_t *counts, const uint64_t *fl
                        const float *recv_scales, const int32_t *recv_meta, const int32_t *tok_slot,
                        int32_t *region_offsets, void *packed_x, float *packed_scales, int32_t *packed_meta,
                        int32_t *tok_packed, int32_t *err, cudaStream_t stream) {
-  ScanArgs sa{counts, flags, region_offsets, err, static_cast<int64_t>(s.E) * s.R, s.max_m};
+  const int64_t nreg = static_cast<int64_t>(s.E) * s.R;
+  const int64_t npacked = s.ntok * s.k;
+  CompactArgs ca{static_cast<const uint8_t *>(recv_x), recv_scales, reinterpret_cast<const int4 *>(recv_meta),
+                 tok_slot, region_offsets, static_cast<uint8_t *>(packed_x), packed_scales,
+                 reinterpret_cast<int4 *>(packed_meta), tok_packed, nreg, npacked, s.T, s.k, s.max_m, s.nsc,
+                 static_cast<uint32_t>(s.row_bytes)};
+  if (nreg <= kRecvMaxRegions) {
+    RecvArgs ra{counts, flags, region_offsets, err, ca, early_trigger(s.ntok)};
+    const size_t smem = static_cast<size_t>(nreg + 1) * sizeof(int32_t);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(recv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess)
+      return MOE_ECUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, recv_kernel, kRecvThreads, smem) != cudaSuccess)
+      return MOE_ECUDA;
+    if (per_sm < 1) return MOE_EINVAL;
+    int64_t grid = static_cast<int64_t>(sm_count()) * per_sm;
+    const int64_t need = (npacked + kRecvWarps - 1) / kRecvWarps;
+    if (grid > need) grid = need > 0 ? need : 1;
+    cudaLaunchConfig_t rc = {};
+    rc.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    rc.blockDim = dim3(kRecvThreads, 1, 1);
+    rc.dynamicSmemBytes = smem;
+    rc.stream = stream;
+    cudaLaunchAttribute ra_attr[1];
+    use_pdl(rc, ra_attr);
+    if (cudaLaunchKernelEx(&rc, recv_kernel, ra) != cudaSuccess) return MOE_ECUDA;
+    return launch_status();
+  }
+  ScanArgs sa{counts, flags, region_offsets, err, nreg, s.max_m};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, 1, 1);
   cfg.blockDim = dim3(kScanThreads, 1, 1);
@@ -163,12 +278,7 @@ moe_status launch_recv(const Sizes &s, const int32_t *counts, const uint64_t *fl
   use_pdl(cfg, attr);
   if (cudaLaunchKernelEx(&cfg, region_scan_kernel, sa) != cudaSuccess) return MOE_ECUDA;
   if (launch_status() != MOE_OK) return MOE_ECUDA;
-  const int64_t npacked = s.ntok * s.k;
   if (npacked == 0) return MOE_OK;
-  CompactArgs ca{static_cast<const uint8_t *>(recv_x), recv_scales, reinterpret_cast<const int4 *>(recv_meta),
-                 tok_slot, region_offsets, static_cast<uint8_t *>(packed_x), packed_scales,
-                 reinterpret_cast<int4 *>(packed_meta), tok_packed, sa.nreg, npacked, s.T, s.k, s.max_m, s.nsc,
-                 static_cast<uint32_t>(s.row_bytes)};
   const int64_t blocks = (npacked + kCompactWarps - 1) / kCompactWarps;
   if (blocks > 0x7fffffffll) return MOE_EINVAL;
   cudaLaunchConfig_t cc = {};
