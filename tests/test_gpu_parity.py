@@ -186,6 +186,57 @@ def test_edge_shapes(name, fused):
     _full_parity(w, wl.make_inputs(w, seed=3), region_sets=small, fused=fused)
 
 
+# Input rows, or slot rows, at 16-byte but not 32-byte alignment: the fused
+# kernel then takes its 16-byte vector forms (for quantised rows, and for plain
+# rows longer than 8 KiB, its generic form). Rows are offset inside larger
+# buffers; the results must equal the oracle's.
+MISALIGNED = {
+    "quant_x": (wl.custom("mis_quant", num_ranks=4, tokens_per_rank=64, hidden=1024, num_experts=32, topk=4,
+                          max_m=64, dtype="bf16q", expert="scale", x_dist="normal"), "x"),
+    "long_rows_recv": (wl.custom("mis_long", num_ranks=2, tokens_per_rank=48, hidden=6144, num_experts=8, topk=2,
+                                 max_m=48, x_dist="normal"), "recv_x"),
+    "fp8_k16_both": (wl.custom("mis_k16", num_ranks=2, tokens_per_rank=40, hidden=1024, num_experts=32, topk=16,
+                               max_m=40, dtype="fp8", expert="scale", x_dist="normal"), "both"),
+}
+
+
+def _offset16(t: torch.Tensor) -> torch.Tensor:
+    """A copy of t whose storage starts 16 bytes past a 256-byte boundary."""
+    nb = t.numel() * t.element_size()
+    raw = torch.empty(nb + 16, dtype=torch.uint8, device=t.device)
+    v = raw[16:16 + nb].view(t.dtype).view(t.shape)
+    v.copy_(t)
+    return v
+
+
+@pytest.mark.parametrize("name", list(MISALIGNED))
+def test_fused_with_16_byte_aligned_rows(name):
+    w, which = MISALIGNED[name]
+    inp = wl.make_inputs(w, seed=9)
+    ref = oracle.run(w, inp)
+    desc = B.MoeDesc.of(w)
+    assert B.moe_layout_dispatch_kernels(desc) == 1
+    bufs = B.allocate_buffers(desc, "cuda:0")
+    if which in ("recv_x", "both"):
+        bufs.recv_x = _offset16(bufs.recv_x)
+    step = P.MoeStep(w, "cuda:0", buffers=bufs)
+    d = P.to_device(inp, "cuda:0")
+    if which in ("x", "both"):
+        d = P.DeviceInputs(d.topk_idx, d.topk_weights, _offset16(d.x), d.x_scales)
+    assert (d.x.data_ptr() % 32 != 0) == (which in ("x", "both"))
+    assert (step.buf.recv_x.data_ptr() % 32 != 0) == (which in ("recv_x", "both"))
+    step.reset()
+    step.layout_dispatch(d)
+    flags = step.buf.flags.clone()
+    step.experts()
+    step.combine(d)
+    assert step.error() == B.MOE_OK
+    ts = check_layout(step, flags, ref, w)
+    check_dispatch(step, w, ts, ref)
+    out = step.buf.out.view(torch.int16).cpu().numpy().view(np.uint16).reshape(w.num_tokens, w.hidden)
+    assert_combine_close(out, ref.out)
+
+
 @pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
 @pytest.mark.parametrize("num_sms", [1, 3])
 def test_few_sms_deep_pipeline(num_sms, fused):
