@@ -184,6 +184,24 @@ def profiled_traffic(kernel_file: str, workload: str):
     return float(m_bytes.group(1))
 
 
+def profiled_dispatch_traffic(workload: str):
+    """DRAM bytes of one layout+dispatch call from the committed per-workload ncu summary, if it was
+    taken on the current layout and dispatch sources."""
+    path = os.path.join(ROOT, "profiles", f"moe_combine_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_bytes = re.search(r"dispatch_dram_bytes_per_step:\s*([0-9.eE+]+)", text)
+    if not m_bytes:
+        return None
+    for name in ("moe_dispatch.cu", "moe_layout.cu", "moe_layout_dispatch.cu"):
+        m = re.search(r"`" + re.escape(name) + r"` ([0-9a-f]+)", text)
+        if not m or m.group(1) != kernel_source_hash(name):
+            return None
+    return float(m_bytes.group(1))
+
+
 # --- native arm -------------------------------------------------------------------
 
 # Throughput configs reported beside the headline workload (the north star's
@@ -269,7 +287,8 @@ def time_config(name, K, W, num_sms, dev, flush, world):
         "roofline": {"kernel": "combine_kernel" if dom == "combine" else "layout+dispatch", "bound": "hbm",
                      "achieved": kernels[dom]["GBps"], "peak": peak, "peak_kind": f"{peak_kind} (copy bandwidth)",
                      "unit": "GB/s", "frac": kernels[dom]["frac_of_measured_hbm"],
-                     "traffic": profiled_traffic("moe_combine.cu", name) if dom == "combine" else None,
+                     "traffic": (profiled_traffic("moe_combine.cu", name) if dom == "combine"
+                                 else profiled_dispatch_traffic(name)),
                      "algorithmic_bytes_per_launch": ab[dom]},
         "gpu_launches": (nk + 1) * K,
         "steps": K,
