@@ -492,6 +492,67 @@ def test_recv_packs_expert_major_and_combine_reads_it(name, fused):
     assert not step.buf.flags.any().item()
 
 
+RECV_REGIONS = {
+    # E * R = 8192 regions: the largest count scan the one-kernel receive hook holds in shared memory
+    "8192_regions": wl.custom("recv8192", num_ranks=32, tokens_per_rank=6, hidden=128, num_experts=256, topk=8,
+                              max_m=6, dtype="fp8", expert="scale", x_dist="normal"),
+    # E * R = 16384 regions: the two-kernel form (one-CTA scan, then compaction)
+    "16384_regions": wl.custom("recv16384", num_ranks=64, tokens_per_rank=5, hidden=128, num_experts=256, topk=8,
+                               max_m=5, dtype="fp8", expert="scale", x_dist="normal"),
+    # E * R = 8196 regions, bf16 rows: just past the one-kernel limit
+    "8196_regions": wl.custom("recv8196", num_ranks=2, tokens_per_rank=40, hidden=64, num_experts=4098, topk=3,
+                              max_m=40),
+    # an empty batch on each form: offsets all zero, nothing packed
+    "empty_one_kernel": wl.custom("recv_empty1", num_ranks=4, tokens_per_rank=0, hidden=128, num_experts=64,
+                                  topk=4, max_m=4),
+    "empty_two_kernels": wl.custom("recv_empty2", num_ranks=2, tokens_per_rank=0, hidden=64, num_experts=4098,
+                                   topk=3, max_m=4),
+}
+
+
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+@pytest.mark.parametrize("masked", [0.0, 0.3], ids=["all", "masked"])
+@pytest.mark.parametrize("name", list(RECV_REGIONS))
+def test_recv_on_both_sides_of_the_one_kernel_region_limit(name, masked, fused):
+    """The receive hook with region counts at and past what its one-kernel form scans
+    in shared memory: offsets, packed rows, scales and headers and the forward map
+    equal the oracle's, and the packed combine equals the slot combine bit for bit."""
+    w = RECV_REGIONS[name]
+    inp = wl.make_inputs(w, seed=3)
+    if masked:
+        inp = wl.mask_choices(inp, masked, seed=4)
+    ref = oracle.run(w, inp)
+    step, d, _, err, _ = run_step(w, inp, fused=fused)
+    assert err == B.MOE_OK, B.moe_status_string(err)
+    out_slots = step.buf.out.clone()
+    packed = B.allocate_packed(step.desc, "cuda:0")
+    packed.packed_meta.fill_(-7)
+    packed.tok_packed.fill_(12345)
+    packed.region_offsets.fill_(-9)
+    if fused:
+        step.layout_dispatch(d)
+    else:
+        step.layout(d)
+        step.dispatch(d)
+    step.recv(packed)
+    assert step.error() == B.MOE_OK
+    off = oracle.region_offsets(ref.counts, w.max_m)
+    assert np.array_equal(packed.region_offsets.cpu().numpy(), off)
+    n = int(off[-1])
+    opk = oracle.compact(ref.slots, off, w.num_ranks, w.num_experts, w.max_m, n)
+    assert np.array_equal(packed.packed_meta[:n].cpu().numpy(), opk.meta)
+    assert np.array_equal(packed.packed_x[:n].cpu().numpy(), opk.rows)
+    if packed.packed_scales is not None:
+        assert np.array_equal(packed.packed_scales[:n].cpu().numpy().view(np.uint32), opk.scales.view(np.uint32))
+    t64 = ref.tok_slot.astype(np.int64)
+    want_tp = np.where(t64 >= 0, off[np.maximum(t64, 0) // w.max_m] + np.maximum(t64, 0) % w.max_m, -1)
+    assert np.array_equal(packed.tok_packed.cpu().numpy(), want_tp)
+    sop = torch.from_numpy(np.sort(t64[t64 >= 0].ravel())).cuda()   # slots in packed order
+    step.combine_packed(d, step.y.index_select(0, sop).contiguous(), packed)
+    assert step.error() == B.MOE_OK
+    assert torch.equal(step.buf.out.view(torch.int16), out_slots.view(torch.int16))
+
+
 def test_recv_without_counts_times_out():
     w = wl.WORKLOADS["tiny"]
     step = P.MoeStep(w, "cuda:0")
