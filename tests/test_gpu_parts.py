@@ -5,7 +5,8 @@ synthetic experts and combine read the parts, and combine clears every part's
 flags. Checked against the oracle (dispatch bit-exact per (source rank,
 token, choice) at the part and local slot the partition rule gives; combine
 within 2^-7 with exact zeros) and against the single-buffer step (identical
-output), for G = 1, 2, 4 and 8, on the fused kernel and on the two-kernel path.
+output), for G = 1, 2, 4 and 8, on the fused kernel and on the two-kernel path, and with combine's
+bulk-TMA form (16384 tokens, k = 4).
 """
 import numpy as np
 import pytest
@@ -30,7 +31,11 @@ CASES = {
     # 1500 tokens per rank: the cluster layout kernel, then the dispatch kernel (bf16, identity experts)
     "two_kernels_bf16": wl.custom("parts_bf16", num_ranks=4, tokens_per_rank=1500, hidden=256, num_experts=16,
                                   topk=4, max_m=1500, x_dist="normal"),
+    # 16384 tokens with k = 4: combine stages its pieces with bulk TMA, reading y from the parts
+    "tma_combine_fp8": wl.custom("parts_tma", num_ranks=8, tokens_per_rank=2048, hidden=256, num_experts=32, topk=4,
+                                 max_m=2048, dtype="fp8", expert="scale", x_dist="normal", renormalize=False),
 }
+TWO_KERNELS = ("two_kernels_bf16", "tma_combine_fp8")
 
 
 @pytest.fixture(autouse=True)
@@ -79,7 +84,7 @@ def test_parts_match_the_oracle_and_the_single_buffer(name, G):
     ref = oracle.run(w, inp)
     pb, guards, counts, tok_slot, flags, out, status = _run_parts(w, inp, G, dev)
     assert status == B.MOE_OK, B.moe_status_string(status)
-    assert B.moe_layout_dispatch_kernels(B.MoeDesc.of(w)) == (2 if name == "two_kernels_bf16" else 1)
+    assert B.moe_layout_dispatch_kernels(B.MoeDesc.of(w)) == (2 if name in TWO_KERNELS else 1)
 
     assert np.array_equal(counts.cpu().numpy(), ref.counts)
     ts = tok_slot.cpu().numpy()
