@@ -144,25 +144,32 @@ struct RecvArgs {
   int early;
 };
 
-// One pass of the 16-byte row copy of packed row p from slot `slot`, shared by
-// both forms of the receive hook.
+// The copy of packed row p from slot `slot` by one warp, shared by both forms
+// of the receive hook. The header and the first scales are loaded first; then
+// each pass has every lane issue up to kCopyBatch 16-byte loads (the last pass
+// of a row predicated, not a run of single dependent load -> store steps)
+// before its stores.
 __device__ __forceinline__ void copy_packed_row(const CompactArgs &a, int64_t p, int64_t slot, int lane) {
   const uint4 *src = reinterpret_cast<const uint4 *>(a.recv_x + slot * a.row_bytes);
   uint4 *dst = reinterpret_cast<uint4 *>(a.packed_x + p * a.row_bytes);
   const uint32_t nv = a.row_bytes / 16;
-  uint32_t v = lane;
-  for (; v + (kCopyBatch - 1) * 32 < nv; v += kCopyBatch * 32) {
+  int4 m = make_int4(0, 0, 0, 0);
+  if (lane == 0) m = a.recv_meta[slot];
+  float sc0 = 0.0f;
+  if (lane < a.nsc) sc0 = a.recv_scales[slot * a.nsc + lane];
+  for (uint32_t v = lane; v < nv; v += kCopyBatch * 32) {
     uint4 t[kCopyBatch];
 #pragma unroll
-    for (int b = 0; b < kCopyBatch; ++b) t[b] = __ldcs(src + v + b * 32);
+    for (int b = 0; b < kCopyBatch; ++b)
+      if (v + b * 32 < nv) t[b] = __ldcs(src + v + b * 32);
 #pragma unroll
-    for (int b = 0; b < kCopyBatch; ++b) dst[v + b * 32] = t[b];
+    for (int b = 0; b < kCopyBatch; ++b)
+      if (v + b * 32 < nv) dst[v + b * 32] = t[b];
   }
-  for (; v < nv; v += 32) dst[v] = __ldcs(src + v);
-  for (int c = lane; c < a.nsc; c += 32) a.packed_scales[p * a.nsc + c] = a.recv_scales[slot * a.nsc + c];
+  if (lane < a.nsc) a.packed_scales[p * a.nsc + lane] = sc0;
+  for (int c = lane + 32; c < a.nsc; c += 32) a.packed_scales[p * a.nsc + c] = a.recv_scales[slot * a.nsc + c];
   if (lane == 0) {
     // the header {src, t, e, j} also gives combine its forward map to the packed row
-    const int4 m = a.recv_meta[slot];
     a.packed_meta[p] = m;
     if (m.y >= 0 && m.y < a.T && m.w >= 0 && m.w < a.k && m.x >= 0 &&
         static_cast<int64_t>(m.x) * a.T * a.k < a.npacked_max)
