@@ -155,6 +155,45 @@ __device__ __forceinline__ uint16_t e4m3x2_rn_satfinite(float lo, float hi) {
   return r;  // lo in the low byte, hi in the high byte
 }
 
+// The block scale of a 128-element block and what the code helper below needs:
+// s = amax / 448 (IEEE fp32; 1 for an all-zero block), r = 1/s rounded to
+// nearest, and r scaled by 1 - 2^-20 and 1 + 2^-20. fast is false where 1/s
+// could leave the normal range (s below 2^-125, or not finite).
+struct BlockScale {
+  float s, lo, hi;
+  bool fast;
+};
+
+__device__ __forceinline__ BlockScale block_scale(float amax) {
+  BlockScale b;
+  b.s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  b.fast = b.s >= 0x1p-125f && b.s <= 0x1p+125f;
+  const float r = __frcp_rn(b.s);
+  b.lo = r * 0x1.ffffep-1f;  // 1 - 2^-20
+  b.hi = r * 0x1.00001p+0f;  // 1 + 2^-20
+  return b;
+}
+
+// The e4m3 codes of x0 / s and x1 / s: the IEEE fp32 quotients, converted with
+// round to nearest even and saturation (low byte x0), in the common case
+// without a division. With r = RN(1/s), three roundings of relative size at
+// most 2^-24 separate x * RN(r (1 - 2^-20)) from x/s (1 - 2^-20), so it lies
+// below x/s by a relative 2^-20 - 3 * 2^-24 or more, and x * RN(r (1 + 2^-20))
+// lies above it by as much. The correctly rounded quotient is within 2^-24 of
+// x/s, so the two products bracket it. The conversion is monotonic: when both
+// products give the same codes, those are the quotient's. Where they differ
+// (an e4m3 rounding boundary within about 2^-20 of the quotient, or a NaN) the
+// quotients are computed by division. Products that fall to fp32 subnormals
+// are below 2^-125 and code 0, as the quotient does.
+__device__ __forceinline__ uint16_t e4m3x2_of_quotients(float x0, float x1, const BlockScale &b) {
+  if (b.fast) {
+    const uint16_t lo = e4m3x2_rn_satfinite(x0 * b.lo, x1 * b.lo);
+    const uint16_t hi = e4m3x2_rn_satfinite(x0 * b.hi, x1 * b.hi);
+    if (lo == hi) return lo;
+  }
+  return e4m3x2_rn_satfinite(__fdiv_rn(x0, b.s), __fdiv_rn(x1, b.s));
+}
+
 __device__ __forceinline__ void quantize_blocks(const uint16_t *src, uint8_t *dst, float *sc, int nblk, int warp,
                                                 int nwarps, int lane) {
   for (int b = warp; b < nblk; b += nwarps) {
@@ -164,11 +203,11 @@ __device__ __forceinline__ void quantize_blocks(const uint16_t *src, uint8_t *ds
     float amax = fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-    const uint32_t q = static_cast<uint32_t>(e4m3x2_rn_satfinite(__fdiv_rn(f0, s), __fdiv_rn(f1, s))) |
-                       (static_cast<uint32_t>(e4m3x2_rn_satfinite(__fdiv_rn(f2, s), __fdiv_rn(f3, s))) << 16);
+    const BlockScale bs = block_scale(amax);
+    const uint32_t q = static_cast<uint32_t>(e4m3x2_of_quotients(f0, f1, bs)) |
+                       (static_cast<uint32_t>(e4m3x2_of_quotients(f2, f3, bs)) << 16);
     *reinterpret_cast<uint32_t *>(dst + b * kScaleBlock + lane * 4) = q;
-    if (lane == 0) sc[b] = s;
+    if (lane == 0) sc[b] = bs.s;
   }
 }
 

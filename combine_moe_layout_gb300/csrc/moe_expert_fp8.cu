@@ -28,7 +28,9 @@
 //   warp 1      owns 512 TMEM columns (two 128 x 256 fp32 partials) and issues
 //               4 MMAs (M 128, N 256 or 128, K 32) per K block into one
 //               partial, alternating partials so the next K block's MMAs run
-//               while the previous partial is promoted. Warps 2-3 idle.
+//               while the previous partial is promoted. It commits once per K
+//               block: the same barrier frees the stage for the producer and
+//               hands the partial to the promotion. Warps 2-3 idle.
 //   warps 4-11  promotion and epilogue: warp w reads TMEM lanes 32 (w % 4) ..
 //               +31 (the tile's rows) and one half of the columns; it adds the
 //               scaled partial into 128 fp32 registers and, after the last K
@@ -81,10 +83,10 @@ constexpr int kF8CtrlRegs = 56;
 constexpr int kF8PromoRegs = 224;
 static_assert(128 * kF8CtrlRegs + 256 * kF8PromoRegs <= kF8Threads * kF8LaunchRegs, "register split over budget");
 constexpr uint32_t kF8TmemCols = 2 * kF8BN;     // two partials
-// stages | epilogue staging (staged form) | full, empty (S each), pfull, pempty (2 each), xbar (4), done |
-// slot, abort | amax exchange
+// stages | epilogue staging (staged form) | full (S), kdone (4), pempty (2), xbar (4), done | slot, abort |
+// amax exchange
 __host__ __device__ constexpr int f8_smem_fixed(int stages, bool staged) {
-  return 1024 + stages * kF8Stage + (staged ? kF8PromoWarps * kF8OutBytes : 0) + (2 * stages + 2 + 2 + 4 + 1) * 8 + 8 +
+  return 1024 + stages * kF8Stage + (staged ? kF8PromoWarps * kF8OutBytes : 0) + (stages + 4 + 2 + 4 + 1) * 8 + 8 +
          2 * 2 * kF8BM * 4;
 }
 constexpr int kF8SmemMax = 227 * 1024;
@@ -164,13 +166,16 @@ template <int STAGES, bool STAGED>
 __global__ void __launch_bounds__(kF8Threads, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                             const __grid_constant__ CUtensorMap map_b1, const F8Args a) {
+  static_assert(STAGES >= 2 && STAGES <= 4, "the producer's stage wait relies on four kdone barriers");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + (((smem_addr(smem_raw) + 1023u) & ~1023u) - smem_addr(smem_raw));
   uint8_t *ostage = smem + STAGES * kF8Stage;  // [promotion warp][kF8OutBytes], staged form only
   uint64_t *full = reinterpret_cast<uint64_t *>(ostage + (STAGED ? kF8PromoWarps * kF8OutBytes : 0));
-  uint64_t *empty = full + STAGES;
-  uint64_t *pfull = empty + STAGES;
-  uint64_t *pempty = pfull + 2;
+  // kdone[i % 4] completes when the MMAs of the CTA's K block i have: it frees
+  // stage i % STAGES for the producer and hands partial i % 2 to the promotion
+  // (one commit per K block)
+  uint64_t *kdone = full + STAGES;
+  uint64_t *pempty = kdone + 4;
   uint64_t *xbar = pempty + 2;
   uint64_t *done = xbar + 4;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
@@ -181,14 +186,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full + s, 1);
-      mbar_init(empty + s, 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(pfull + b, 1);
-      mbar_init(pempty + b, kF8PromoWarps);
-    }
+    for (int s = 0; s < STAGES; ++s) mbar_init(full + s, 1);
+    for (int b = 0; b < 4; ++b) mbar_init(kdone + b, 1);
+    for (int b = 0; b < 2; ++b) mbar_init(pempty + b, kF8PromoWarps);
     for (int q = 0; q < 4; ++q) mbar_init(xbar + q, 64);  // every lane of the two warps of a row quarter
     mbar_init(done, 1);
     *abort = 0;
@@ -225,8 +225,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         const Tile t = tile_of<kF8BM>(w, pref, offs, a);
         const int brow = t.e * a.expert_rows + t.n0;
         for (int kb = 0; kb < kblocks; ++kb) {
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-          if (!role_wait(empty + s, ph ^ 1u, abort, a.err)) {
+          const uint32_t s = it % STAGES;
+          // the stage is free once the MMAs of K block it - STAGES have completed
+          // (STAGES <= 4: that barrier cannot have moved on to K block it yet)
+          if (it >= STAGES && !role_wait(kdone + ((it - STAGES) & 3u), ((it - STAGES) >> 2) & 1u, abort, a.err)) {
             ok = false;
             break;
           }
@@ -267,11 +269,14 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           tc_fence_after();
           const uint32_t sa = smem_addr(smem + s * kF8Stage), sb = sa + kF8TileA;
           const uint32_t d = tmem_base + pb * kF8BN;
+          // K step kk starts kk * 32 bytes further along the swizzled rows: the
+          // descriptor's address field (bits 0-13, address >> 4) grows by 2 per step
+          const uint64_t da = sw128_desc(sa), db = sw128_desc(sb);
 #pragma unroll
           for (int kk = 0; kk < kF8BK / kF8UK; ++kk)
-            mma_e4m3(d, sw128_desc(sa + kk * kF8UK), sw128_desc(sb + kk * kF8UK), idesc, kk != 0);
-          mma_commit(smem_addr(empty + s));
-          mma_commit(smem_addr(pfull + pb));
+            mma_e4m3(d, da + static_cast<uint64_t>(kk * kF8UK / 16), db + static_cast<uint64_t>(kk * kF8UK / 16), idesc,
+                     kk != 0);
+          mma_commit(smem_addr(kdone + (it & 3u)));
           ++it;
           ++pk;
         }
@@ -321,10 +326,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
         const float f0 = sa * sb;
         const float f1 = sw ? sa * sb2 : f0;
-        const uint32_t pb = pk & 1u, pph = (pk >> 1) & 1u;
+        const uint32_t pb = pk & 1u;
         // every lane polls the barrier (measured 2-3% faster than one lane and a
         // broadcast); the vote keeps the warp together if a bounded wait gives up
-        const bool got = __all_sync(0xffffffffu, role_wait(pfull + pb, pph, abort, a.err));
+        const bool got = __all_sync(0xffffffffu, role_wait(kdone + (pk & 3u), (pk >> 2) & 1u, abort, a.err));
         if (!got) {
           ok = false;
           break;
@@ -364,7 +369,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         mbar_arrive_local(xbar + q);
         if (!__all_sync(0xffffffffu, role_wait(xbar + q, static_cast<uint32_t>(lt & 1), abort, a.err))) break;
         const float amax = fmaxf(part, slot[(j ^ 1) * kF8BM + m]);
-        const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+        const BlockScale bs = block_scale(amax);
+        const float sc = bs.s;
         if constexpr (STAGED) {
           // this lane's 64 codes into its staging row (64 bytes: four 16-byte pieces,
           // piece p at p ^ ((row >> 1) & 3), so that eight rows fill all 32 banks)
@@ -375,8 +381,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int x = 16 * v + 4 * i;
-              const uint16_t lo = e4m3x2_rn_satfinite(__fdiv_rn(acc[x], sc), __fdiv_rn(acc[x + 1], sc));
-              const uint16_t hi = e4m3x2_rn_satfinite(__fdiv_rn(acc[x + 2], sc), __fdiv_rn(acc[x + 3], sc));
+              const uint16_t lo = e4m3x2_of_quotients(acc[x], acc[x + 1], bs);
+              const uint16_t hi = e4m3x2_of_quotients(acc[x + 2], acc[x + 3], bs);
               pk4[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
             }
             buf[lane * 4 + (v ^ ((lane >> 1) & 3))] = make_uint4(pk4[0], pk4[1], pk4[2], pk4[3]);
@@ -398,8 +404,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             uint32_t pk4[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const uint16_t lo = e4m3x2_rn_satfinite(__fdiv_rn(acc[4 * i], sc), __fdiv_rn(acc[4 * i + 1], sc));
-              const uint16_t hi = e4m3x2_rn_satfinite(__fdiv_rn(acc[4 * i + 2], sc), __fdiv_rn(acc[4 * i + 3], sc));
+              const uint16_t lo = e4m3x2_of_quotients(acc[4 * i], acc[4 * i + 1], bs);
+              const uint16_t hi = e4m3x2_of_quotients(acc[4 * i + 2], acc[4 * i + 3], bs);
               pk4[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
             }
             uint8_t *orow = static_cast<uint8_t *>(a.out) + arow * a.n_total + t.n0 + 64 * j;

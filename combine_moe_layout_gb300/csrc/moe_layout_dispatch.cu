@@ -106,8 +106,12 @@ __device__ __forceinline__ void st_row(uint8_t *p, const RowVec<W> &r, uint64_t 
   }
 }
 
+// The quantising forms would take up to 96 registers a thread, 5 CTAs per SM:
+// 760 of a decode batch's 1024 rows at a time, then a second wave. Capped at 72
+// (7 CTAs per SM, every row of the batch at once, a few words spilled), the
+// 1024-row bf16 decode batch measured 20.3 against 24.3 us.
 template <int W, int VPT, int KC, bool QUANT>
-__global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArgs a) {
+__global__ void __launch_bounds__(kFusedThreads, QUANT ? 7 : 1) layout_dispatch_kernel(FusedArgs a) {
   __shared__ int32_t s_part[kFusedWarps][KC];
   __shared__ int32_t s_own[KC];
   __shared__ int32_t s_slot[KC];
@@ -272,8 +276,10 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
       // Quantise on dispatch. Vector q holds bf16 elements (W/2)q .. (W/2)q +
       // W/2 - 1, so a 128-element block is G = 256 / W consecutive lanes (vin is
       // a multiple of G). scale = amax / 448 (1 for an all-zero block), code =
-      // e4m3(x / scale) with IEEE fp32 division and the hardware's nearest-even
-      // saturating conversion; W/2 codes per thread.
+      // e4m3(x / scale): the code of the IEEE fp32 quotient under the hardware's
+      // nearest-even saturating conversion, found without a division unless the
+      // quotient sits near an e4m3 rounding boundary (e4m3x2_of_quotients); W/2
+      // codes per thread.
       constexpr int NE = W / 2;         // bf16 elements per vector
       constexpr int G = 256 / W;        // lanes per 128-element block
 #pragma unroll
@@ -290,13 +296,13 @@ __global__ void __launch_bounds__(kFusedThreads) layout_dispatch_kernel(FusedArg
         for (int p = 0; p < NE; ++p) amax = fmaxf(amax, fabsf(f[p]));
 #pragma unroll
         for (int o = G / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+        const BlockScale bs = block_scale(amax);
+        const float s = bs.s;
         uint32_t c[NE / 4];
 #pragma unroll
         for (int p = 0; p < NE / 4; ++p)
-          c[p] = static_cast<uint32_t>(e4m3x2_rn_satfinite(__fdiv_rn(f[4 * p], s), __fdiv_rn(f[4 * p + 1], s))) |
-                 (static_cast<uint32_t>(e4m3x2_rn_satfinite(__fdiv_rn(f[4 * p + 2], s), __fdiv_rn(f[4 * p + 3], s)))
-                  << 16);
+          c[p] = static_cast<uint32_t>(e4m3x2_of_quotients(f[4 * p], f[4 * p + 1], bs)) |
+                 (static_cast<uint32_t>(e4m3x2_of_quotients(f[4 * p + 2], f[4 * p + 3], bs)) << 16);
         // 16-byte stores: 32-byte vectors give 16 codes each; 16-byte vectors
         // give 8, so even lanes take their odd neighbour's 8 as well
         RowVec<16> out16;

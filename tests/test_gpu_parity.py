@@ -418,6 +418,44 @@ def test_ds_decode_bf16_rows_quantised_on_dispatch(fused):
     assert step.buf.recv_x.shape[1] == w.hidden
 
 
+def _e4m3_boundary_rows(R, T, H, seed=9):
+    """bf16 rows whose 128-element blocks have amax = 448 * 2^e (so the scale is 2^e exactly) and whose other
+    elements are e4m3 rounding boundaries times 2^e (exact ties, the subnormal midpoints and 2^-10), their bf16
+    neighbours and negatives: x / scale lands on or next to a boundary, where the quotient decides the code."""
+    rng = np.random.default_rng(seed)
+    mids = [(1 + (2 * m + 1) / 16) * 2.0 ** e for e in range(-6, 9) for m in range(8)]
+    mids += [(j + 0.5) * 2.0 ** -9 for j in range(7)] + [2.0 ** -10, 2.0 ** -7]
+    mids = np.array(mids, dtype=np.float32)
+    bits = mids.view(np.uint32) >> 16  # exact in bf16: at most 5 significant bits
+    cand = np.concatenate([bits, bits + 1, bits - 1]).astype(np.uint32)
+    cand = cand[(cand << 16).view(np.float32) < 448.0]  # below the block's amax
+    nblk = R * T * H // 128
+    e = rng.integers(-20, 21, size=nblk)
+    vals = rng.choice(cand, size=(nblk, 128)).astype(np.uint32)
+    vals[:, 0] = np.float32(448.0).view(np.uint32) >> 16
+    # scale by 2^e: add e to the bf16 exponent field (every value stays normal)
+    vals = (vals + (e[:, None] << 7).astype(np.int64)).astype(np.uint32)
+    vals |= (rng.integers(0, 2, size=(nblk, 128)) << 15).astype(np.uint32)  # random signs
+    vals[:, 0] &= 0x7FFF
+    return vals.astype(np.uint16).reshape(R, T, H)
+
+
+@pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
+def test_quantised_dispatch_at_e4m3_rounding_boundaries(fused):
+    """Quotients x / scale exactly on e4m3 rounding boundaries (ties to even, the subnormal midpoints, 2^-10) and
+    one bf16 step either side: the slot codes and scales equal the oracle's, which divides in fp32."""
+    w = wl.custom("qties", num_ranks=2, tokens_per_rank=100, hidden=1024, num_experts=8, topk=2, max_m=100,
+                  dtype="bf16q", expert="scale", renormalize=False)
+    inp = wl.make_inputs(w)
+    inp.x = _e4m3_boundary_rows(w.num_ranks, w.tokens_per_rank, w.hidden)
+    # the inputs do put quotients on boundaries: every block's scale is a power of two
+    xf = (inp.x.astype(np.uint32) << 16).view(np.float32).reshape(-1, 128)
+    q = np.abs(xf) / (np.abs(xf).max(axis=1, keepdims=True) / np.float32(448))
+    m = (q.view(np.uint32) & 0xFFFFF) == 0x80000
+    assert m.mean() > 0.2, "most quotients sit exactly on a tie"
+    _full_parity(w, inp, fused=fused)
+
+
 @pytest.mark.parametrize("fused", FUSED, ids=FUSED_IDS)
 @pytest.mark.parametrize("num_sms", [1, 4])
 def test_quantised_dispatch_deep_pipeline(num_sms, fused):
