@@ -109,9 +109,12 @@ __device__ __forceinline__ void st_row(uint8_t *p, const RowVec<W> &r, uint64_t 
 // The quantising forms would take up to 96 registers a thread, 5 CTAs per SM:
 // 760 of a decode batch's 1024 rows at a time, then a second wave. Capped at 72
 // (7 CTAs per SM, every row of the batch at once, a few words spilled), the
-// 1024-row bf16 decode batch measured 20.3 against 24.3 us.
+// 1024-row bf16 decode batch measured 20.3 against 24.3 us. The other forms
+// give 0, which leaves the register count to the compiler as with no bound (an
+// explicit 1 let it grow the fp8 decode form from 62 to 100 registers, 4 CTAs
+// per SM, and that step from 36.8 to 38.3 us).
 template <int W, int VPT, int KC, bool QUANT>
-__global__ void __launch_bounds__(kFusedThreads, QUANT ? 7 : 1) layout_dispatch_kernel(FusedArgs a) {
+__global__ void __launch_bounds__(kFusedThreads, QUANT ? 7 : 0) layout_dispatch_kernel(FusedArgs a) {
   __shared__ int32_t s_part[kFusedWarps][KC];
   __shared__ int32_t s_own[KC];
   __shared__ int32_t s_slot[KC];
