@@ -204,8 +204,8 @@ def profiled_dispatch_traffic(workload: str):
 
 # --- native arm -------------------------------------------------------------------
 
-# Throughput configs reported beside the headline workload (the benchmark spec's
-# prefill target and the other large shapes).
+# Throughput configs reported beside the headline workload (the DeepSeek-shape
+# prefill batch and the other large shapes).
 PER_CONFIG = ("ds_prefill", "mixtral", "skewed")
 
 
