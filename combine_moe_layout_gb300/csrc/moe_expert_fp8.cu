@@ -158,6 +158,14 @@ __device__ __forceinline__ void fma2(float f, uint32_t p0, uint32_t p1, float &a
       : "f"(f), "r"(p0), "r"(p1));
 }
 
+// A 2-D TMA tensor store of one box from shared memory, in the CTA's bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_local(uint64_t *bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
@@ -165,7 +173,8 @@ __device__ __forceinline__ void mbar_arrive_local(uint64_t *bar) {
 template <int STAGES, bool STAGED>
 __global__ void __launch_bounds__(kF8Threads, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
-                            const __grid_constant__ CUtensorMap map_b1, const F8Args a) {
+                            const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_y,
+                            const F8Args a) {
   static_assert(STAGES >= 2 && STAGES <= 4, "the producer's stage wait relies on four kdone barriers");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + (((smem_addr(smem_raw) + 1023u) & ~1023u) - smem_addr(smem_raw));
@@ -421,13 +430,19 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
       } else if constexpr (STAGED) {
         // bf16 y, 64 columns at a time: this lane's 128 bytes into its staging row
-        // (piece p at p ^ (row & 7)), then stores of 4 rows x 128 bytes, whole lines:
-        // lane l takes piece l % 8 of row l / 8 + 4 i
+        // (piece p at p ^ (row & 7): the layout of a TMA box with the 128-byte
+        // swizzle). A warp whose 32 rows all belong to the tile stores them with
+        // one TMA tensor store and goes on; otherwise the lanes store 4 rows x 128
+        // bytes at a time, whole lines: lane l takes piece l % 8 of row l / 8 + 4 i
         uint4 *buf = reinterpret_cast<uint4 *>(ostage + (warp - 4) * kF8OutBytes);
         __nv_bfloat16 *obase = static_cast<__nv_bfloat16 *>(a.out) + t.n0 + cbase;
+        const bool whole = q * 32 + 31 < t.rows;
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           if (2 * h2 < ncol) {
+            // the staging rows are free once the last tensor store has read them
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
 #pragma unroll
             for (int p = 0; p < 8; ++p) {
               uint32_t pk2[4];
@@ -439,13 +454,23 @@ __global__ void __launch_bounds__(kF8Threads, 1)
               }
               buf[lane * 8 + (p ^ (lane & 7))] = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
             }
-            __syncwarp();
+            if (whole) {
+              fence_proxy_async_smem();  // the rows written above, before the async proxy reads them
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&map_y, smem_addr(buf), t.n0 + cbase + 64 * h2, t.row0 + q * 32);
+                bulk_commit();
+              }
+            } else {
+              __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int r = (lane >> 3) + 4 * i, p = lane & 7;
-              const uint4 v = buf[r * 8 + (p ^ (r & 7))];
-              if (q * 32 + r < t.rows)
-                reinterpret_cast<uint4 *>(obase + static_cast<int64_t>(t.row0 + q * 32 + r) * a.n_total + 64 * h2)[p] = v;
+              for (int i = 0; i < 8; ++i) {
+                const int r = (lane >> 3) + 4 * i, p = lane & 7;
+                const uint4 v = buf[r * 8 + (p ^ (r & 7))];
+                if (q * 32 + r < t.rows)
+                  reinterpret_cast<uint4 *>(obase + static_cast<int64_t>(t.row0 + q * 32 + r) * a.n_total + 64 * h2)[p] =
+                      v;
+              }
             }
             __syncwarp();
           }
@@ -471,6 +496,11 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
       }
     }
+    // the tensor stores issued from this warp's staging rows have completed
+    if constexpr (STAGED) {
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -478,6 +508,19 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kF8TmemCols);
   }
+}
+
+// 2-D map of the bf16 [rows][cols] output: boxes of 32 rows x 64 columns (128 bytes), 128-byte swizzle.
+bool make_map_y(CUtensorMap *map, const void *base, int64_t cols, int64_t rows) {
+  const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int fp8_group_width(const F8Args &a, int concurrent) {
@@ -489,7 +532,7 @@ int fp8_group_width(const F8Args &a, int concurrent) {
 
 template <int STAGES, bool STAGED>
 moe_status launch_form(const F8Args &a, const CUtensorMap &ma, const CUtensorMap &mb0, const CUtensorMap &mb1,
-                       int64_t grid, cudaStream_t stream) {
+                       const CUtensorMap &my, int64_t grid, cudaStream_t stream) {
   auto kernel = grouped_gemm_fp8_kernel<STAGES, STAGED>;
   const int smem = f8_smem_fixed(STAGES, STAGED) + 12 * (a.E + 1);  // offsets + two class prefixes
   if (smem > kF8SmemMax) return MOE_EINVAL;
@@ -505,7 +548,7 @@ moe_status launch_form(const F8Args &a, const CUtensorMap &ma, const CUtensorMap
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   use_pdl(cfg, attr);
-  if (cudaLaunchKernelEx(&cfg, kernel, ma, mb0, mb1, a) != cudaSuccess) return MOE_ECUDA;
+  if (cudaLaunchKernelEx(&cfg, kernel, ma, mb0, mb1, my, a) != cudaSuccess) return MOE_ECUDA;
   return launch_status();
 }
 
@@ -518,15 +561,21 @@ moe_status launch_fp8(F8Args a, const void *A, const void *B0, const void *B1, i
   if (max_tiles > INT32_MAX) return MOE_EINVAL;
   const int sms = num_sms > 0 ? num_sms : sm_count();
   a.group_n = fp8_group_width(a, sms);
-  CUtensorMap ma, mb0, mb1;
+  CUtensorMap ma, mb0, mb1, my;
   if (!make_map(&ma, A, a.K, a.rows, 1) || !make_map(&mb0, B0, a.K, b_total_rows, 1) ||
       !make_map(&mb1, B1, a.K, b_total_rows, 1))
+    return MOE_ECUDA;
+  // linear 2's bf16 output [rows][n_total]: boxes of 32 rows x 64 columns with the 128-byte swizzle, the
+  // layout of a promotion warp's staging rows (gate/up writes h with plain stores and never uses the map)
+  if (a.swiglu)
+    my = ma;
+  else if (!make_map_y(&my, a.out, a.n_total, a.rows))
     return MOE_ECUDA;
   const int64_t grid = max_tiles < sms ? max_tiles : sms;
   if (grid <= 0) return MOE_OK;
   // fewer expected rows per expert than one tile: the weight stream bounds the launch
-  if (a.rows / a.E < kF8BM) return launch_form<4, false>(a, ma, mb0, mb1, grid, stream);
-  return launch_form<3, true>(a, ma, mb0, mb1, grid, stream);
+  if (a.rows / a.E < kF8BM) return launch_form<4, false>(a, ma, mb0, mb1, my, grid, stream);
+  return launch_form<3, true>(a, ma, mb0, mb1, my, grid, stream);
 }
 
 moe_status check_fp8(const moe_desc *desc, int32_t inter, Sizes *s, int64_t *rows) {
