@@ -90,3 +90,34 @@ def test_receive_plans_of_two_parts_cover_every_entry_once():
     valid = {(s, t, j) for s, t, j in zip(*np.nonzero(tok_slot >= 0))}
     assert set(seen) == valid, "every routed entry lands in exactly one part; masked ones in none"
     assert len(valid) < tok_slot.size, "the case includes masked choices"
+
+
+def test_part_rule_on_the_host():
+    """The host rule, single process: the parts must divide the ranks; part g holds global slots
+    [g P, (g + 1) P) at local slot s - g P; G = 1 is the whole buffer; every plan's entries and local slots
+    agree with the rule, and the union of the G plans is every routed entry exactly once."""
+    import pytest
+    sys.path.insert(0, ROOT)
+    import oracle
+    from combine_moe_layout_gb300 import parts
+
+    with pytest.raises(ValueError):
+        parts.slots_per_part(4, 16, 8, 3)
+    with pytest.raises(ValueError):
+        parts.slots_per_part(4, 16, 8, 0)
+    assert parts.slots_per_part(4, 16, 8, 1) == 16 * 4 * 8
+    g, loc = parts.part_of_slot(np.array([0, 127, 128, 511]), 128)
+    assert g.tolist() == [0, 0, 1, 3] and loc.tolist() == [0, 127, 0, 127]
+    w, inp = _case()
+    _, _, tok_slot = oracle.layout(inp.topk_idx, w.num_experts, w.max_m)
+    for G in (1, 2, 4):
+        P = parts.slots_per_part(w.num_ranks, w.num_experts, w.max_m, G)
+        seen = 0
+        for g in range(G):
+            plan = parts.receive_plan(tok_slot, w.num_experts, w.max_m, G, g)
+            src, t, j = plan.entries.T
+            s = tok_slot[src, t, j].astype(np.int64)
+            assert (s // P == g).all() and np.array_equal(s % P, plan.local_slots)
+            assert plan.regions.size == w.num_experts * w.num_ranks // G
+            seen += plan.entries.shape[0]
+        assert seen == int((tok_slot >= 0).sum())
