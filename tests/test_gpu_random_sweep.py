@@ -16,6 +16,8 @@ bands. Every case checks, against the oracle:
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -56,6 +58,9 @@ def _cases(n: int = 64, seed: int = 20261202):
 
 
 CASES = _cases()
+# MOE_SWEEP_SEEDS="7,99,2027" adds 64 more cases per seed (a longer sweep; the default run keeps one seed)
+for _seed in [int(x) for x in os.environ.get("MOE_SWEEP_SEEDS", "").split(",") if x.strip()]:
+    CASES += [(f"c{_seed * 1000 + int(c[0][1:])}",) + c[1:] for c in _cases(seed=_seed)]
 
 
 @pytest.mark.parametrize("name,case,masked,fused,num_sms", CASES, ids=[c[0] for c in CASES])
